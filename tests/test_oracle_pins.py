@@ -1,0 +1,670 @@
+"""Pins for the CPU oracle, against things other than the oracle itself.
+
+Each test checks an oracle function against one of: values printed by the
+SGLang pull-request digests (tests/golden/pages_constants.json), the OCP E4M3
+specification (tests/golden/e4m3_spec_points.txt), a library routine (torch's
+float8 / bfloat16 conversions, numpy reductions), a closed form, a brute-force
+search on tiny inputs, or an invariant the definition implies. No expected value
+comes from the CUDA library.
+"""
+import itertools
+import json
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def pages():
+    with open(os.path.join(GOLD, "pages_constants.json")) as f:
+        return json.load(f)
+
+
+def torch_e4m3(v32: np.ndarray) -> np.ndarray:
+    """Library routine: torch's float32 -> float8_e4m3fn (RNE for |v| <= 448)."""
+    return torch.from_numpy(np.ascontiguousarray(v32, np.float32)).to(
+        torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def torch_bf16(v32: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(np.ascontiguousarray(v32, np.float32)).to(
+        torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def bf16_to_f32(b):
+    return synth.from_bf16_bits(b)
+
+
+# ---------------------------------------------------------------------------
+# e4m3 (OCP spec)
+# ---------------------------------------------------------------------------
+
+def test_e4m3_spec_points(ref):
+    rows = []
+    with open(os.path.join(GOLD, "e4m3_spec_points.txt")) as f:
+        for line in f:
+            line = line.split("#")[0].strip()
+            if line:
+                v, c = line.split()
+                rows.append((float(v), int(c, 16)))
+    vals = np.array([v for v, _ in rows])
+    codes = np.array([c for _, c in rows], np.uint8)
+    assert (ref.e4m3_encode(vals) == codes).all()
+    dec = ref.e4m3_decode(codes)
+    assert np.array_equal(dec, vals)
+    assert np.array_equal(np.signbit(dec), np.signbit(vals))
+
+
+def test_e4m3_code_table_properties(ref):
+    codes = np.arange(256, dtype=np.uint8)
+    v = ref.e4m3_decode(codes)
+    nan = np.isnan(v)
+    assert set(np.flatnonzero(nan)) == {0x7F, 0xFF}
+    pos = v[:0x7F]
+    assert (np.diff(pos) > 0).all(), "codes 0..126 strictly increasing"
+    assert pos[-1] == 448.0 and pos[1] == 2.0 ** -9 and pos[8] == 2.0 ** -6
+    finite = codes[~nan]
+    assert (ref.e4m3_encode(v[~nan]) == finite).all(), "encode(decode(c)) == c"
+
+
+def test_e4m3_encode_matches_library_rne(ref):
+    codes = np.arange(0x7F)
+    v = ref.e4m3_decode(codes.astype(np.uint8))
+    mids = (v[:-1] + v[1:]) / 2.0                       # exact ties
+    mids32 = mids.astype(np.float32)
+    assert np.array_equal(mids32.astype(np.float64), mids)
+    near = np.concatenate([np.nextafter(mids32, np.float32(0)), np.nextafter(mids32, np.float32(1e9))])
+    rng = np.random.default_rng(7)
+    rand = np.concatenate([rng.uniform(0, 448, 20000), np.exp(rng.uniform(-16, 6, 20000)),
+                           rng.uniform(0, 2 ** -6, 5000)]).astype(np.float32)
+    allv = np.concatenate([v.astype(np.float32), mids32, near, rand])
+    allv = allv[np.abs(allv) <= 448]
+    allv = np.concatenate([allv, -allv])
+    got = ref.e4m3_encode(allv.astype(np.float64))
+    assert np.array_equal(got, torch_e4m3(allv))
+
+
+def test_e4m3_saturates(ref):
+    assert ref.e4m3_encode(np.array([449.0, 1e6, -500.0])).tolist() == [0x7E, 0x7E, 0xFE]
+
+
+def test_bf16_rne_matches_library(ref):
+    rng = np.random.default_rng(3)
+    f = np.concatenate([rng.standard_normal(20000).astype(np.float32),
+                        (rng.integers(0, 2 ** 16, 5000).astype(np.uint32) << 16 | 0x8000).view(np.float32),
+                        np.array([0.0, -0.0, 1e-40, 3.0e38], np.float32)])
+    f = f[np.isfinite(f)]
+    got = np.array([ref.bf16_rne(float(a)) for a in f], np.uint16)
+    assert np.array_equal(got, torch_bf16(f))
+
+
+# ---------------------------------------------------------------------------
+# Group exponent (direct UE8M0 quantisation, PR #33128 实现拆解 item 3)
+# ---------------------------------------------------------------------------
+
+def all_positive_bf16():
+    bits = np.arange(1, 0x7F80, dtype=np.uint32)
+    return (bits << 16).view(np.float32)
+
+
+def test_group_exponent_interval_exact(ref):
+    """For every positive finite bf16 amax: 448*2^(e-1) < max(amax, eps) <= 448*2^e."""
+    a = all_positive_bf16()
+    e = ref.group_exponent(a)
+    eps = float(np.float32(1e-10))
+    for av, ev in zip(a[::7].tolist(), e[::7].tolist()):
+        x = Fraction(max(av, eps))
+        hi = Fraction(448) * (Fraction(2) ** ev)
+        lo = hi / 2
+        assert lo < x <= hi, (av, ev)
+
+
+def test_group_exponent_equals_fp32_division_reading(ref):
+    """Second reading: e = ceil(log2(fl32(amax / 448))) with an IEEE fp32
+    division (numpy). The two coincide on every positive finite bf16."""
+    a = all_positive_bf16()
+    q = np.maximum(a, np.float32(1e-10)) / np.float32(448.0)   # fp32 division
+    m, ex = np.frexp(q.astype(np.float64))                        # q = m * 2^ex, m in [0.5, 1)
+    ceil_log2 = np.where(m == 0.5, ex - 1, ex)
+    assert np.array_equal(ref.group_exponent(a), ceil_log2.astype(np.int32))
+
+
+def test_group_exponent_closed_forms(ref):
+    for k in range(-30, 110):
+        a = np.float32(448.0 * 2.0 ** k)
+        nxt = np.nextafter(a, np.float32(np.inf))
+        nb = (np.array([a], np.float32).view(np.uint32) + (1 << 16)).view(np.float32)  # next bf16
+        assert ref.group_exponent(np.array([a, nxt, nb[0]], np.float32)).tolist() == [k, k + 1, k + 1]
+    # all-zero group: eps = 1e-10 -> e = -42 (448 * 2^-42 = 1.0186e-10 >= 1e-10 > 448 * 2^-43)
+    assert ref.group_exponent(np.array([0.0, 1e-12, 1e-10], np.float32)).tolist() == [-42, -42, -42]
+
+
+# ---------------------------------------------------------------------------
+# Row quantisation
+# ---------------------------------------------------------------------------
+
+def graded_row(rng, H, g):
+    """bf16 row whose groups have very different magnitudes (so a wrong group
+    index or a transposed scale shows up)."""
+    x = rng.standard_normal(H).astype(np.float32)
+    gain = 2.0 ** ((np.arange(H) // g) % 9 - 4).astype(np.float32)
+    return synth.to_bf16_bits(x * gain)
+
+
+@pytest.mark.parametrize("g,H", [(128, 256), (128, 640), (32, 224), (128, 7168), (32, 7168)])
+def test_quant_row_against_library(ref, g, H):
+    rng = np.random.default_rng(H + g)
+    for _ in range(4):
+        x = graded_row(rng, H, g)
+        q, eb = ref.quant_row(x, g)
+        xf = bf16_to_f32(x).reshape(-1, g)
+        e = eb.astype(np.int32) - 127
+        amax = np.abs(xf).max(axis=1)
+        # scale choice: amax / 2^e in (224, 448]
+        ratio = amax.astype(np.float64) / np.ldexp(1.0, e)
+        assert ((ratio > 224) & (ratio <= 448)).all()
+        # payload: the library's RNE of x * 2^-e (exact in fp32 here)
+        scaled = (xf.astype(np.float64) * np.ldexp(1.0, -e)[:, None]).astype(np.float32)
+        assert np.array_equal(q.reshape(-1, g), torch_e4m3(scaled))
+
+
+def test_quant_row_zero_group(ref):
+    x = np.zeros(256, np.uint16)
+    x[128:] = synth.to_bf16_bits(np.linspace(-3, 3, 128, dtype=np.float32))
+    x[5] = 0x8000  # -0
+    q, eb = ref.quant_row(x, 128)
+    assert eb[0] == 85 and q[5] == 0x80 and (np.delete(q[:128], 5) == 0).all()
+
+
+# ---------------------------------------------------------------------------
+# Layout choice and compact bound (PR #33128 code excerpts)
+# ---------------------------------------------------------------------------
+
+def test_masked_rule_truth_table(ref):
+    p = pages()
+    lim = p["masked_local_expert_limit"]["value"]
+    assert lim == 32
+    cases = {(256, 32): True, (256, 33): False, (8, 8): False, (256, 256): False,
+             (64, 16): True, (33, 32): True, (32, 32): False, (512, 1): True}
+    for (E, L), want in cases.items():
+        assert ref.should_use_masked(E, L) == want
+
+
+def brute_force_bound(A, L, b):
+    best = 0
+    for c in itertools.product(range(A + 1), repeat=L):
+        if sum(c) <= A:
+            best = max(best, sum(-(-ci // b) * b for ci in c))
+    return best
+
+
+def test_compact_bound_brute_force(ref):
+    for A in range(0, 10):
+        for L in range(1, 5):
+            for b in (1, 2, 3, 4):
+                assert ref.compact_bound(A, L, b) == brute_force_bound(A, L, b), (A, L, b)
+
+
+def test_compact_bound_workloads(ref):
+    assert pages()["compact_block_e_default"]["value"] == 128
+    assert ref.compact_bound(16 * 2, 8, 128) == 1024
+    assert ref.compact_bound(8192 * 8, 256, 128) == 98048
+    # tight: L-1 experts with one row each, the rest on one expert
+    A, L, b = 1000, 7, 16
+    c = [1] * (L - 1) + [A - (L - 1)]
+    assert sum(-(-x // b) * b for x in c) == ref.compact_bound(A, L, b)
+
+
+# ---------------------------------------------------------------------------
+# Dispatch layouts
+# ---------------------------------------------------------------------------
+
+def packed_to_rows(buf_u8, rows, G, ld, blocks=1):
+    """Read a packed column-major scale buffer back as [rows, 4*G4] bytes with
+    numpy reshapes / transposes (an independent reading of the layout)."""
+    G4 = (G + 3) // 4
+    rpb = rows // blocks
+    words = buf_u8.view(np.int32).reshape(blocks, G4, ld)
+    t = np.ascontiguousarray(words.transpose(0, 2, 1)[:, :rpb, :])   # [blocks, rpb, G4] words
+    return t.view(np.uint8).reshape(blocks * rpb, G4 * 4)           # little-endian bytes
+
+
+def run_compact(ref, x, ids, w, H, K, L, b, g, fmt, n_live=None):
+    T = ids.shape[0]
+    n_live = T if n_live is None else n_live
+    bound = ref.compact_bound(T * K, L, b)
+    G = H // g
+    xq = np.full((bound, H), 0xEE, np.uint8)
+    sc, ld = ref.scale_buffer(fmt, bound, G)
+    mi = np.full(bound, -7, np.int32)
+    s2d = np.full((T, K), -9, np.int32)
+    counts = np.full(L, -5, np.int32); starts = counts.copy(); psum = counts.copy()
+    total = np.zeros(1, np.int32)
+    rw = np.full(bound, np.nan, np.float32)
+    st = ref.dispatch_compact(x, T, n_live, H, ids, w, K, L, b, g, fmt, xq, sc, ld, mi, bound,
+                              s2d, counts, starts, psum, total, rw)
+    return dict(st=st, bound=bound, xq=xq, sc=sc, ld=ld, mi=mi, s2d=s2d, counts=counts,
+                starts=starts, psum=psum, total=int(total[0]), rw=rw)
+
+
+def check_compact_invariants(ref, r, ids, x, w, H, K, L, b, g, fmt, n_live):
+    T = ids.shape[0]
+    flat = ids.reshape(-1)
+    live = np.repeat(np.arange(T) < n_live, K)
+    kept = live & (flat >= 0) & (flat < L)
+    assert np.array_equal(r["counts"], np.bincount(flat[kept], minlength=L)[:L])
+    s, p, c = r["starts"], r["psum"], r["counts"]
+    assert s[0] == 0 and (s % b == 0).all() and np.array_equal(p - s, c)
+    assert (s[1:] >= p[:-1]).all() and (s[1:] - p[:-1] < b).all(), "densest aligned segments"
+    assert r["total"] % b == 0 and r["total"] >= p[-1] and r["total"] - p[-1] < b
+    assert r["total"] <= r["bound"]
+    s2d = r["s2d"].reshape(-1)
+    assert (s2d[~kept] == -1).all()
+    rows = s2d[kept]
+    assert len(np.unique(rows)) == len(rows), "src2dst injective"
+    e = flat[kept]
+    assert ((rows >= s[e]) & (rows < p[e])).all()
+    for ee in range(L):      # stable: rows of an expert increase with t*K + k
+        re = rows[e == ee]
+        assert (np.diff(re) > 0).all()
+    want_mi = np.full(r["bound"], -1, np.int32)
+    want_mi[rows] = e
+    assert np.array_equal(r["mi"], want_mi)
+    G = H // g
+    untouched = np.ones(r["bound"], bool)
+    untouched[rows] = False
+    assert (r["xq"][untouched] == 0xEE).all(), "padding rows never written"
+    assert np.isnan(r["rw"][untouched]).all()
+    if fmt == "packed":
+        sc_rows = packed_to_rows(r["sc"], r["bound"] + (-r["bound"]) % 4, G, r["ld"])[: r["bound"]]
+    elif fmt == "u8":
+        sc_rows = r["sc"]
+    else:
+        sc_rows = None
+    for a in np.flatnonzero(kept):
+        t = a // K
+        q, eb = ref.quant_row(x[t], g)
+        row = s2d[a]
+        assert np.array_equal(r["xq"][row], q)
+        assert r["rw"][row] == w.reshape(-1)[a]
+        if fmt == "f32":
+            assert np.array_equal(r["sc"][row, :G], np.ldexp(1.0, eb.astype(np.int32) - 127).astype(np.float32))
+        else:
+            assert np.array_equal(sc_rows[row, :G], eb)
+            if fmt == "packed":
+                assert (sc_rows[row, G:] == 0).all(), "packed pad bytes are zero"
+
+
+@pytest.mark.parametrize("fmt", ["packed", "u8", "f32"])
+def test_dispatch_compact_invariants_random(ref, fmt):
+    for seed in range(3):
+        d = synth.tiny(seed, T=37, H=640)
+        x, ids, w = d["x"], d["topk_ids"], d["topk_weights"]
+        ids = ids.copy()
+        ids[3, 0] = -1
+        ids[5, 1] = 99          # not a local expert: dropped
+        r = run_compact(ref, x, ids, w, 640, 2, 8, 16, 128, fmt, n_live=33)
+        assert r["st"] == 0
+        check_compact_invariants(ref, r, ids, x, w, 640, 2, 8, 16, 128, fmt, 33)
+
+
+def test_dispatch_compact_exhaustive_tiny(ref):
+    """Every routing of T<=3 tokens x K<=2 slots over ids {-1, 0..L-1, L}."""
+    H, g = 128, 128
+    rng = np.random.default_rng(11)
+    n = 0
+    for T, K, L in [(1, 1, 1), (2, 1, 2), (1, 2, 3), (2, 2, 2), (3, 2, 1), (3, 1, 3)]:
+        x = synth.to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+        w = rng.random((T, K)).astype(np.float32)
+        for combo in itertools.product(range(-1, L + 1), repeat=T * K):
+            ids = np.array(combo, np.int32).reshape(T, K)
+            r = run_compact(ref, x, ids, w, H, K, L, 2, g, "packed")
+            check_compact_invariants(ref, r, ids, x, w, H, K, L, 2, g, "packed", T)
+            n += 1
+    assert n > 1000
+
+
+def run_masked(ref, x, ids, w, H, K, L, cap, g, fmt, n_live=None):
+    T = ids.shape[0]
+    n_live = T if n_live is None else n_live
+    G = H // g
+    xq = np.full((L * cap, H), 0xEE, np.uint8)
+    sc, ld = ref.scale_buffer(fmt, L * cap, G, blocks=L)
+    mm = np.full(L, -5, np.int32)
+    s2d = np.full((T, K), -9, np.int32)
+    rw = np.full(L * cap, np.nan, np.float32)
+    st = ref.dispatch_masked(x, T, n_live, H, ids, w, K, L, cap, g, fmt, xq, sc, ld, mm, s2d, rw)
+    return dict(st=st, xq=xq, sc=sc, ld=ld, mm=mm, s2d=s2d, rw=rw)
+
+
+@pytest.mark.parametrize("fmt", ["packed", "u8"])
+def test_dispatch_masked_invariants(ref, fmt):
+    d = synth.decode(0, T=24)
+    H = 640
+    x = d["x"][:, :H].copy()
+    ids, w = d["topk_ids"], d["topk_weights"]
+    K, L, cap, g = 8, 32, 16, 128
+    r = run_masked(ref, x, ids, w, H, K, L, cap, g, fmt)
+    flat = ids.reshape(-1)
+    kept = (flat >= 0) & (flat < L)
+    cnt = np.bincount(flat[kept], minlength=L)
+    assert np.array_equal(r["mm"], np.minimum(cnt, cap))
+    assert r["st"] == (1 if (cnt > cap).any() else 0)
+    s2d = r["s2d"].reshape(-1)
+    assert (s2d[~kept] == -1).all()
+    rows = s2d[kept]
+    e = flat[kept]
+    ok = rows >= 0
+    assert (rows[ok] // cap == e[ok]).all()
+    assert len(np.unique(rows[ok])) == ok.sum()
+    for ee in range(L):
+        re = rows[(e == ee) & ok]
+        assert np.array_equal(re % cap, np.arange(len(re))), "rank order, no gaps"
+    G = H // g
+    sc_rows = packed_to_rows(r["sc"], L * cap, G, r["ld"], blocks=L) if fmt == "packed" else r["sc"]
+    for a in np.flatnonzero(kept):
+        row = s2d[a]
+        if row < 0:
+            continue
+        q, eb = ref.quant_row(x[a // K], g)
+        assert np.array_equal(r["xq"][row], q)
+        assert np.array_equal(sc_rows[row, :G], eb)
+    untouched = np.ones(L * cap, bool)
+    untouched[rows[ok]] = False
+    assert (r["xq"][untouched] == 0xEE).all()
+
+
+def test_dispatch_masked_overflow(ref):
+    T, K, L, cap, H = 10, 1, 4, 6, 128
+    ids = np.zeros((T, K), np.int32)
+    ids[8:, 0] = 1
+    x = synth.to_bf16_bits(np.random.default_rng(0).standard_normal((T, H)).astype(np.float32))
+    w = np.ones((T, K), np.float32)
+    r = run_masked(ref, x, ids, w, H, K, L, cap, 128, "u8")
+    assert r["st"] & ref.ST_OVERFLOW
+    assert r["mm"].tolist() == [6, 2, 0, 0]
+    assert r["s2d"][:, 0].tolist() == [0, 1, 2, 3, 4, 5, -1, -1, 6, 7]
+    # exactly at capacity: no overflow
+    r = run_masked(ref, x[:8], ids[:8], w[:8], H, K, L, 8, 128, "u8")
+    assert r["st"] == 0 and r["mm"].tolist() == [8, 0, 0, 0]
+
+
+def test_masked_and_compact_combine_identical(ref):
+    """PR #33128 test idea: masked and compact layouts give the same end result.
+    Expert outputs are a function of (expert, token) only, so the combine must
+    agree bit for bit across layouts."""
+    d = synth.decode(1, T=40)
+    H, K, L, cap, g = 256, 8, 32, 40, 128
+    x = d["x"][:, :H].copy()
+    ids, w = d["topk_ids"], d["topk_weights"]
+    T = ids.shape[0]
+    rc = run_compact(ref, x, ids, w, H, K, L, 128, g, "packed")
+    rm = run_masked(ref, x, ids, w, H, K, L, cap, g, "packed")
+    assert rm["st"] == 0
+    rng = np.random.default_rng(5)
+    table = synth.to_bf16_bits(rng.standard_normal((L, T, H)).astype(np.float32))
+    yc = np.zeros((rc["bound"], H), np.uint16)
+    ym = np.zeros((L * cap, H), np.uint16)
+    for a in range(T * K):
+        e, t = ids.reshape(-1)[a], a // K
+        if 0 <= e < L:
+            yc[rc["s2d"].reshape(-1)[a]] = table[e, t]
+            ym[rm["s2d"].reshape(-1)[a]] = table[e, t]
+    oc = ref.combine_f32(yc, rc["s2d"], w, T, K, H)
+    om = ref.combine_f32(ym, rm["s2d"], w, T, K, H)
+    assert np.array_equal(oc, om)
+
+
+# ---------------------------------------------------------------------------
+# Combine
+# ---------------------------------------------------------------------------
+
+def test_combine_f64_against_numpy(ref):
+    rng = np.random.default_rng(2)
+    T, K, H, R = 50, 4, 96, 300
+    y = synth.to_bf16_bits(rng.standard_normal((R, H)).astype(np.float32))
+    s2d = rng.integers(-1, R, size=(T, K)).astype(np.int32)
+    w = rng.random((T, K)).astype(np.float32)
+    out, mass = ref.combine_f64(y, s2d, w, T, K, H)
+    yf = bf16_to_f32(y).astype(np.float64)
+    g = np.where(s2d[..., None] >= 0, yf[np.maximum(s2d, 0)], 0.0)       # [T,K,H]
+    want = np.einsum("tk,tkh->th", w.astype(np.float64), g)
+    assert np.allclose(out, want, rtol=1e-13, atol=1e-13)
+    assert np.allclose(mass, np.einsum("tk,tkh->th", w.astype(np.float64), np.abs(g)), rtol=1e-13)
+
+
+def test_combine_f32_error_bound_and_edge_cases(ref):
+    rng = np.random.default_rng(4)
+    T, K, H, R = 64, 8, 128, 512
+    y = synth.to_bf16_bits(rng.standard_normal((R, H)).astype(np.float32))
+    s2d = rng.integers(-1, R, size=(T, K)).astype(np.int32)
+    s2d[0] = -1                                   # all dropped -> zeros
+    w = synth.softmax_weights(rng, T, K)
+    o32 = ref.combine_f32(y, s2d, w, T, K, H)
+    o64, mass = ref.combine_f64(y, s2d, w, T, K, H)
+    assert (o32[0] == 0).all()
+    of = bf16_to_f32(o32).astype(np.float64)
+    ulp = np.ldexp(1.0, np.frexp(np.abs(o64))[1] - 8)      # bf16 ulp at |ref|
+    tol = ulp + K * 2.0 ** -24 * mass
+    assert (np.abs(of - o64) <= tol).all()
+    # K = 1, w = 1: an exact copy of the source row
+    s1 = rng.integers(0, R, size=(T, 1)).astype(np.int32)
+    o = ref.combine_f32(y, s1, None, T, 1, H)
+    assert np.array_equal(o, y[s1[:, 0]])
+
+
+# ---------------------------------------------------------------------------
+# Requant (PR #14162)
+# ---------------------------------------------------------------------------
+
+def test_requant_against_library(ref):
+    d = synth.requant(0, T=64, H=256)
+    q, s = d["q"], d["s_tok"]
+    out, S = ref.requant(q, s, 64, 256)
+    assert S == float(s.max())
+    r = (s / np.float32(S)).astype(np.float32)                      # fp32 division
+    dq = ref.e4m3_decode(q).astype(np.float32)
+    v = (dq * r[:, None]).astype(np.float32)                        # fp32 product
+    assert np.array_equal(out, torch_e4m3(v))
+    tmax = int(np.argmax(s))
+    assert np.array_equal(out[tmax], q[tmax]), "the row holding S is unchanged"
+    err = np.abs(ref.e4m3_decode(out) * S - ref.e4m3_decode(q) * s[:, None].astype(np.float64))
+    a = np.abs(v.astype(np.float64))
+    half_ulp = np.where(a < 2.0 ** -6, 2.0 ** -10, np.ldexp(1.0, np.frexp(a)[1] - 5))
+    assert (err <= S * (half_ulp + 2.0 ** -22 * a) + 1e-30).all()
+
+
+def test_requant_hand_cases(ref):
+    q = np.array([[0x38, 0xC0, 0x00, 0x7E], [0x38, 0x44, 0x80, 0x7E]], np.uint8)  # 1, -2, 0, 448 / 1, 3, -0, 448
+    s = np.array([2.0, 1.0], np.float32)
+    out, S = ref.requant(q, s, 2, 4)
+    assert S == 2.0
+    assert out[0].tolist() == q[0].tolist()
+    assert out[1].tolist() == [0x30, 0x3C, 0x80, 0x76]   # 0.5, 1.5, -0, 224
+    out, S = ref.requant(q, np.zeros(2, np.float32), 2, 4)
+    assert S == 1.0 and out.tolist() == [[0, 0x80, 0, 0], [0, 0, 0x80, 0]]
+    out, S = ref.requant(np.zeros((0, 4), np.uint8), np.zeros(0, np.float32), 0, 4)
+    assert S == 1.0 and out.shape == (0, 4)
+
+
+# ---------------------------------------------------------------------------
+# Expanded <-> masked slab (PR #29525)
+# ---------------------------------------------------------------------------
+
+def build_layout(counts, align, H):
+    """The digest's _build_layout idea, written fresh: expert e occupies
+    [align(psum[e-1]), psum[e]); every real row gets a distinct value
+    ((s + j) % 200 + 1) with an alternating x1 / x2 column gain."""
+    starts, psum, prev = [], [], 0
+    for c in counts:
+        st = -(-prev // align) * align
+        starts.append(st)
+        psum.append(st + c)
+        prev = st + c
+    total = max(-(-prev // align) * align, 1)
+    base = np.zeros((total, H), np.float32)
+    gain = 1.0 + (np.arange(H) % 2)
+    for st, c in zip(starts, counts):
+        for j in range(c):
+            base[st + j] = float((st + j) % 200 + 1) * gain
+    return base, np.array(psum, np.int32), starts, total
+
+
+@pytest.mark.parametrize("counts", [[3, 0, 5, 1], [0, 0, 0, 0], [0, 17, 0, 0], [8, 8, 8, 8], [1, 0, 0, 9]])
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+def test_repack_roundtrip(ref, counts, dtype):
+    p = pages()
+    assert p["psum_alignment"]["value"] == 128
+    H, align, cap, L = 64, 4, 8, len(counts)
+    base, psum, starts, R = build_layout(counts, align, H)
+    if dtype == "bf16":
+        exp = synth.to_bf16_bits(base).view(np.uint8).reshape(R, 2 * H)
+        eb = 2
+    else:
+        exp = torch_e4m3(np.minimum(base, 448)).reshape(R, H)
+        eb = 1
+    slab = np.full((L * cap, H * eb), 0xEE, np.uint8)
+    mm = np.full(L, -1, np.int32)
+    st = ref.expand_to_slab(exp, eb, H, R, None, 0, psum, L, align, cap, "u8", 128, slab, None, 0, mm)
+    over = any(c > cap for c in counts)
+    assert bool(st & ref.ST_OVERFLOW) == over
+    assert mm.tolist() == [min(c, cap) for c in counts], "masked_m equals the real counts"
+    for e, (s0, c) in enumerate(zip(starts, counts)):
+        for j in range(cap):
+            row = slab[e * cap + j]
+            if j < c:
+                assert np.array_equal(row, exp[s0 + j])
+            else:
+                assert (row == 0xEE).all(), "slab padding untouched"
+    back = np.full_like(exp, 0xDD)
+    mi = np.full(R, 77, np.int32)
+    st2 = ref.expand_from_slab(slab, eb, H, None, 0, psum, L, align, cap, "u8", 128, None,
+                               back, R, None, 0, mi)
+    assert bool(st2 & ref.ST_OVERFLOW) == over
+    for e, (s0, c) in enumerate(zip(starts, counts)):
+        for j in range(c):
+            if j < cap:
+                assert np.array_equal(back[s0 + j], exp[s0 + j])
+    real = np.zeros(R, bool)
+    for s0, c in zip(starts, counts):
+        real[s0:s0 + min(c, cap)] = True
+    assert (back[~real] == 0xDD).all(), "expanded padding untouched"
+    want_mi = np.full(R, -1, np.int32)
+    for e, (s0, c) in enumerate(zip(starts, counts)):
+        want_mi[s0:s0 + c] = e
+    assert np.array_equal(mi, want_mi)
+
+
+def test_repack_weighted_rows(ref):
+    counts = [3, 0, 2]
+    H, align, cap, L = 32, 4, 4, 3
+    base, psum, starts, R = build_layout(counts, align, H)
+    exp = synth.to_bf16_bits(base).view(np.uint8).reshape(R, 2 * H)
+    slab = np.zeros((L * cap, 2 * H), np.uint8)
+    mm = np.zeros(L, np.int32)
+    ref.expand_to_slab(exp, 2, H, R, None, 0, psum, L, align, cap, "u8", 128, slab, None, 0, mm)
+    w = np.random.default_rng(0).random(R).astype(np.float32)
+    back = np.full_like(exp, 0xDD)
+    ref.expand_from_slab(slab, 2, H, None, 0, psum, L, align, cap, "u8", 128, w, back, R, None, 0, None)
+    for s0, c in zip(starts, counts):
+        for j in range(c):
+            r = s0 + j
+            want = torch_bf16(w[r] * bf16_to_f32(exp[r].view(np.uint16)))   # fp32 product, RNE
+            assert np.array_equal(back[r].view(np.uint16), want)
+    real = np.zeros(R, bool)
+    for s0, c in zip(starts, counts):
+        real[s0:s0 + c] = True
+    assert (back[~real] == 0xDD).all()
+
+
+@pytest.mark.parametrize("fmt", ["packed", "u8", "f32"])
+def test_repack_scales_from_quantizer(ref, fmt):
+    """PR #29525 review lesson: use scales made by the real quantiser, and a
+    hidden size whose group count does not divide the packing (H=640 -> 5 groups)."""
+    H, g, align, cap = 640, 128, 8, 16
+    counts = [5, 0, 16, 3, 9]
+    L = len(counts)
+    G = H // g
+    _, psum, starts, R = build_layout(counts, align, H)
+    rng = np.random.default_rng(9)
+    x = np.stack([graded_row(rng, H, g) for _ in range(R)])
+    exp = np.zeros((R, H), np.uint8)
+    esc, ld_es = ref.scale_buffer(fmt, R, G)
+    ref.quant_group(x, R, R, H, g, fmt, exp, esc, ld_es)
+    slab = np.full((L * cap, H), 0xEE, np.uint8)
+    ssc, ld_ss = ref.scale_buffer(fmt, L * cap, G, fill=0x5A, blocks=L)
+    mm = np.zeros(L, np.int32)
+    st = ref.expand_to_slab(exp, 1, H, R, esc, ld_es, psum, L, align, cap, fmt, g, slab, ssc, ld_ss, mm)
+    assert st == 0
+    if fmt == "packed":
+        er = packed_to_rows(esc, R + (-R) % 4, G, ld_es)[:R]
+        sr = packed_to_rows(ssc, L * cap, G, ld_ss, blocks=L)
+    else:
+        er, sr = esc, ssc
+    for e, (s0, c) in enumerate(zip(starts, counts)):
+        for j in range(c):
+            assert np.array_equal(sr[e * cap + j, :G], er[s0 + j, :G])
+            assert np.array_equal(slab[e * cap + j], exp[s0 + j])
+    back = np.full_like(exp, 0xDD)
+    bsc, _ = ref.scale_buffer(fmt, R, G, fill=0x33)
+    st = ref.expand_from_slab(slab, 1, H, ssc, ld_ss, psum, L, align, cap, fmt, g, None, back, R, bsc, ld_es, None)
+    assert st == 0
+    for s0, c in zip(starts, counts):
+        assert np.array_equal(back[s0:s0 + c], exp[s0:s0 + c])
+    if fmt == "packed":
+        br = packed_to_rows(bsc, R + (-R) % 4, G, ld_es)[:R]
+    else:
+        br = bsc
+    for s0, c in zip(starts, counts):
+        assert np.array_equal(br[s0:s0 + c, :G], er[s0:s0 + c, :G])
+
+
+def test_repack_bad_layout_flagged(ref):
+    H, L, align, cap = 16, 3, 4, 8
+    psum = np.array([3, 2, 9], np.int32)        # expert 1 ends before its start
+    exp = np.zeros((12, H), np.uint8)
+    slab = np.zeros((L * cap, H), np.uint8)
+    mm = np.zeros(L, np.int32)
+    assert ref.expand_to_slab(exp, 1, H, 12, None, 0, psum, L, align, cap, "u8", 128, slab, None, 0, mm) & ref.ST_BAD_LAYOUT
+    psum = np.array([3, 6, 20], np.int32)       # beyond the buffer
+    assert ref.expand_to_slab(exp, 1, H, 12, None, 0, psum, L, align, cap, "u8", 128, slab, None, 0, mm) & ref.ST_BAD_LAYOUT
+
+
+# ---------------------------------------------------------------------------
+# MXFP8 live-row quantisation (PR #36119)
+# ---------------------------------------------------------------------------
+
+def test_mxfp8_contract_constants(ref):
+    p = pages()
+    g, H = p["mxfp8_group_size"]["value"], p["mxfp8_hidden"]["value"]
+    assert H % g == 0 and H // g == p["mxfp8_scale_dim"]["value"] == 224
+    assert ref.scale_bytes("u8", 1, H, g) == 224 * p["e8m0_itemsize_bytes"]["value"]
+    assert ref.scale_bytes("u8", 0, H, g) == 0
+    sc, ld = ref.scale_buffer("u8", 0, H // g)
+    assert tuple(sc.shape) == tuple(p["empty_live_batch_scale_shape"]["value"])
+    assert torch.empty((0, 224), dtype=torch.float8_e8m0fnu).element_size() == 1
+
+
+def test_quant_group_live_rows_only(ref):
+    d = synth.mxfp8(0, T_cap=64, n_live=5, H=256)
+    x = d["x"]
+    H, g = 256, 32
+    xq = np.full((64, H), 0xEE, np.uint8)
+    sc, ld = ref.scale_buffer("u8", 64, H // g)
+    st = ref.quant_group(x, 64, 5, H, g, "u8", xq, sc, ld)
+    assert st == 0
+    assert (xq[5:] == 0xEE).all() and (sc[5:] == 0xA5).all()
+    for t in range(5):
+        q, eb = ref.quant_row(x[t], g)
+        assert np.array_equal(xq[t], q) and np.array_equal(sc[t], eb)
+    clean = synth.mxfp8(1, T_cap=64, n_live=64, H=256)["x"]
+    st = ref.quant_group(clean, 64, 65, H, g, "u8", xq, sc, ld)
+    assert st & ref.ST_LIVE_OVERFLOW
+    st = ref.quant_group(x, 64, 0, H, g, "u8", np.full((64, H), 1, np.uint8), sc, ld)
+    assert st == 0
