@@ -1,0 +1,503 @@
+"""Benchmark of the MoE permute + FP8 group-quant + combine hot path on GB300.
+
+One step = one compact dispatch (route plan + group-128 UE8M0 quantisation +
+scatter + m_indices) followed by one top-k weighted combine, on the prefill
+workload: T = 8192 tokens, hidden 7168, 256 local experts, top-8 routing with a
+Zipf(1.2) popularity and >= 10 empty experts, block_e = 128, packed UE8M0
+scales. The metric is algorithmic bytes moved per second (dispatch + combine),
+with the dispatch and combine figures, routed tokens/s, the roofline of the
+dominant kernel against the measured HBM copy bandwidth, the CPU oracle as a
+reported baseline, and the other hot-path rows timed on their own workloads.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+For N > 1 launch with torchrun; every rank runs an independent replica of the
+workload (no collective on the data path) and rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "dispatch+quant & combine GB/s and % of GB300 HBM peak; routed tokens/s"
+UNIT = "GB/s"
+WORKLOAD = "prefill compact: T=8192 H=7168 E=L=256 top8 Zipf(1.2) block_e=128 g128 packed-UE8M0"
+L2_FLUSH_BYTES = 512 << 20
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes (what the definition must read and write, once)
+# ---------------------------------------------------------------------------
+
+def dispatch_bytes(T, H, K, L, b, g, kept):
+    """x read once; ids read; payload + packed scales written per kept slot;
+    m_indices over the static bound; src2dst written."""
+    G = H // g
+    bound = b * (min(T * K, L) + (T * K - min(T * K, L)) // b)
+    return (T * H * 2 + T * K * 4 + kept * H + kept * ((G + 3) // 4) * 4 + bound * 4 + T * K * 4)
+
+
+def combine_bytes(T, H, K, kept):
+    """one bf16 row read per kept slot; src2dst and weights read; out written."""
+    return kept * H * 2 + T * K * 4 + T * K * 4 + T * H * 2
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks sampling
+# ---------------------------------------------------------------------------
+
+class Clocks:
+    def __init__(self, gpu_index: int):
+        self.path = tempfile.mktemp(suffix=".csv")
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.f = open(self.path, "w")
+            self.p = subprocess.Popen(["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={q}",
+                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.p.terminate()
+        self.p.wait()
+        self.f.close()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [s.strip() for s in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle baseline (bounded sample of the same workload)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(tokens: int, reps: int):
+    import oracle as ref
+    d = synth.prefill(0)
+    c = d["cfg"]
+    T, H, K, L, b, g = tokens, c["H"], c["K"], c["L"], c["block_e"], c["g"]
+    x, ids, w = d["x"][:T].copy(), d["topk_ids"][:T].copy(), d["topk_weights"][:T].copy()
+    bound = ref.compact_bound(T * K, L, b)
+    y = synth.expert_outputs(np.random.default_rng(11), bound, H)
+    xq = np.zeros((bound, H), np.uint8)
+    sc, ld = ref.scale_buffer("packed", bound, H // g)
+    mi = np.zeros(bound, np.int32)
+    s2d = np.zeros((T, K), np.int32)
+    cnt, st, ps = (np.zeros(L, np.int32) for _ in range(3))
+    tot = np.zeros(1, np.int32)
+    kept = int(((ids >= 0) & (ids < L)).sum())
+    nbytes = dispatch_bytes(T, H, K, L, b, g, kept) + combine_bytes(T, H, K, kept)
+    times = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        ref.dispatch_compact(x, T, T, H, ids, w, K, L, b, g, "packed", xq, sc, ld, mi, bound, s2d,
+                             cnt, st, ps, tot)
+        ref.combine_f32(y, s2d, w, T, K, H)
+        times.append(time.perf_counter() - t0)
+    t = statistics.median(times)
+    return dict(value=nbytes / t / 1e9, unit=UNIT, cores=1, kind="oracle",
+                sample=f"first {T} of 8192 prefill tokens (all H=7168 columns), dispatch + "
+                       f"combine, median of {reps}, single-threaded C oracle",
+                seconds=t, tokens_per_s=T / t)
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the oracle as it stands, on host cores
+# ---------------------------------------------------------------------------
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    sample_tokens = 512
+    for _ in range(args.warmup):
+        oracle_sample(sample_tokens, 1)
+    vals, secs = [], []
+    for _ in range(args.steps):
+        r = oracle_sample(sample_tokens, 1)
+        vals.append(r["value"])
+        secs.append(r["seconds"])
+    v = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": statistics.median(secs) * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16->e4m3",
+        "data": "synthetic (seeded numpy: Zipf top-8 routing, N(0,1) activations)",
+        "config": {"workload": WORKLOAD, "sample_tokens_per_step": sample_tokens,
+                   "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"first {sample_tokens} prefill tokens per step, dispatch + combine"},
+        "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import combine_fp8_quant_gb300 as mp
+    from combine_fp8_quant_gb300 import build as cuda_build
+
+    if rank == 0:
+        cuda_build.build()
+    if world > 1:
+        dist.barrier()
+    mp.load()
+    dev = torch.device(f"cuda:{local_rank}")
+    torch.cuda.set_device(dev)
+
+    d = synth.prefill(rank)
+    c = d["cfg"]
+    T, H, K, E, L, b, g = c["T"], c["H"], c["K"], c["E"], c["L"], c["block_e"], c["g"]
+    x_h = torch.from_numpy(d["x"].view(np.int16)).view(torch.bfloat16)
+    ids_h = torch.from_numpy(d["topk_ids"])
+    w_h = torch.from_numpy(d["topk_weights"])
+    x, ids, w = x_h.to(dev), ids_h.to(dev), w_h.to(dev)
+    bound = mp.moe_compact_bound(T * K, L, b)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(7000 + rank)
+    y = torch.randn((bound, H), generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    kept = int(((d["topk_ids"] >= 0) & (d["topk_ids"] < L)).sum())
+    db = dispatch_bytes(T, H, K, L, b, g, kept)
+    cb = combine_bytes(T, H, K, kept)
+
+    ws = mp.Workspace(T, K, L, dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    xq = torch.empty((bound, H), dtype=torch.uint8, device=dev)
+    sc, ld = mp.scale_tensor("packed", bound, H, g, dev)
+    mi = torch.empty(bound, dtype=torch.int32, device=dev)
+    s2d = torch.empty((T, K), dtype=torch.int32, device=dev)
+    cnt, sts, ps = (torch.empty(L, dtype=torch.int32, device=dev) for _ in range(3))
+    tot = torch.empty(1, dtype=torch.int32, device=dev)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def dispatch(xx, ii):
+        code = mp.moe_dispatch_compact(xx, H, T, None, H, ii, None, K, E, L, b, g, "packed", xq, sc,
+                                       ld, mi, bound, s2d, cnt, sts, ps, tot, None, ws.buf,
+                                       ws.nbytes, st)
+        assert code == 0, code
+
+    def combine(yy, ww, oo):
+        code = mp.moe_combine(yy, H, bound, s2d, ww, T, None, K, H, oo, st)
+        assert code == 0, code
+
+    # -- device-resident timing ----------------------------------------------
+    for _ in range(max(args.warmup, 3)):
+        dispatch(x, ids)
+        combine(y, w, out)
+    torch.cuda.synchronize()
+    assert mp.moe_status_sync(st) == 0
+    K_steps = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K_steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = Clocks(torch.cuda.current_device() if world == 1 else local_rank)
+    for i in range(K_steps):
+        flush.zero_()                       # L2 flush between timed steps (outside the events)
+        ev[i][0].record()
+        dispatch(x, ids)
+        ev[i][1].record()
+        combine(y, w, out)
+        ev[i][2].record()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    t_disp = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K_steps)]
+    t_comb = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K_steps)]
+    t_step = [a + bb for a, bb in zip(t_disp, t_comb)]
+    ms_step = sum(t_step) / K_steps
+    ms_disp = sum(t_disp) / K_steps
+    ms_comb = sum(t_comb) / K_steps
+    if world > 1:
+        tt = torch.tensor([ms_step, ms_disp, ms_comb], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_step, ms_disp, ms_comb = tt.tolist()
+    assert mp.moe_status_sync(st) == 0
+
+    # -- end to end through the C ABI with host buffers -------------------------
+    x_p, ids_p, w_p = x_h.pin_memory(), ids_h.pin_memory(), w_h.pin_memory()
+    y_p = y.cpu().pin_memory()
+    out_p = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+    x2, ids2, w2, y2 = torch.empty_like(x), torch.empty_like(ids), torch.empty_like(w), torch.empty_like(y)
+    h2d = x_p.numel() * 2 + ids_p.numel() * 4 + w_p.numel() * 4 + y_p.numel() * 2
+    d2h = out_p.numel() * 2
+
+    def e2e_step():
+        x2.copy_(x_p, non_blocking=True)
+        ids2.copy_(ids_p, non_blocking=True)
+        w2.copy_(w_p, non_blocking=True)
+        y2.copy_(y_p, non_blocking=True)
+        dispatch(x2, ids2)
+        combine(y2, w2, out)
+        out_p.copy_(out, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_steps = max(3, min(K_steps, 10))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record()
+    torch.cuda.synchronize()
+    ms_e2e = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        tt = torch.tensor([ms_e2e], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_e2e = tt.item()
+
+    # -- other hot-path rows on their own workloads --------------------------------
+    rows = other_rows(mp, dev, flush) if rank == 0 else None
+
+    if rank != 0:
+        return
+    hbm, peak_kind = peaks()
+    step_bytes = (db + cb) * world
+    value = step_bytes / (ms_step * 1e-3) / 1e9
+    comb_gbs = cb / (ms_comb * 1e-3) / 1e9
+    disp_gbs = db / (ms_disp * 1e-3) / 1e9
+    traffic = load_traffic("combine")
+    cpu = oracle_sample(2048, 3)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K_steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16->e4m3 (u8), fp32 accumulate",
+        "data": "synthetic (seeded: numpy Zipf top-8 routing and N(0,1) x; torch N(0,1) expert outputs)",
+        "config": {"workload": WORKLOAD, "T": T, "H": H, "K": K, "E": E, "L": L, "block_e": b,
+                   "group": g, "scales": "packed UE8M0", "bound_rows": bound,
+                   "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write, outside the events)",
+                   "parallelism": f"replicas x{world} (no collective on the data path)"},
+        "detail": {
+            "dispatch": {"us": ms_disp * 1e3, "gbs": disp_gbs, "frac_of_peak": disp_gbs / hbm,
+                         "algorithmic_bytes": db, "launches": 2},
+            "combine": {"us": ms_comb * 1e3, "gbs": comb_gbs, "frac_of_peak": comb_gbs / hbm,
+                        "algorithmic_bytes": cb, "launches": 1},
+            "routed_tokens_per_s": T * world / (ms_step * 1e-3),
+            "dispatch_tokens_per_s": T / (ms_disp * 1e-3),
+            "assignments_per_s": kept * world / (ms_step * 1e-3),
+            "frac_of_nominal_8TBs": value / world / 8000.0,
+        },
+        "roofline": {"bound": "hbm", "kernel": "combine_kernel", "achieved": comb_gbs, "peak": hbm,
+                     "unit": "GB/s", "frac": comb_gbs / hbm, "traffic": traffic,
+                     "peak_source": f"{peak_kind} hbm_gbs (copy, burst)"},
+        "roofline_dispatch": {"bound": "hbm", "kernel": "route_plan + quant_scatter",
+                              "achieved": disp_gbs, "peak": hbm, "unit": "GB/s",
+                              "frac": disp_gbs / hbm, "traffic": load_traffic("dispatch")},
+        "cpu_baseline": {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")},
+        "e2e": {"value": step_bytes / (ms_e2e * 1e-3) / 1e9, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e,
+                "api": "moe_dispatch_compact + moe_combine (C ABI), pinned host buffers"},
+        "gpu_launches": 3 * K_steps,
+        "clocks": clk,
+        "rows": rows,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def load_traffic(which):
+    """DRAM bytes per launch from the committed ncu summary, if one matches the
+    current kernels (null otherwise)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    return d.get(which)
+
+
+def time_call(fn, flush, reps=20):
+    import torch
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    return statistics.median(ts) * 1e3  # us
+
+
+def other_rows(mp, dev, flush):
+    """Decode (masked) dispatch + slab->expand + combine, MXFP8 live-row quant,
+    requant and expand->slab, each on its own workload (median of 20, L2
+    flushed before each call)."""
+    import torch
+    hbm, _ = peaks()
+    res = {}
+
+    def entry(us, nbytes):
+        gbs = nbytes / (us * 1e-6) / 1e9
+        return {"us": us, "gbs": gbs, "frac_of_peak": gbs / hbm, "algorithmic_bytes": nbytes}
+
+    # decode, masked layout
+    dd = synth.decode(0)
+    c = dd["cfg"]
+    T, H, K, E, L, cap, g = c["T"], c["H"], c["K"], c["E"], c["L"], c["cap"], c["g"]
+    x = torch.from_numpy(dd["x"].view(np.int16)).to(dev).view(torch.bfloat16)
+    ids = torch.from_numpy(dd["topk_ids"]).to(dev)
+    w = torch.from_numpy(dd["topk_weights"]).to(dev)
+    ws = mp.Workspace(T, K, L, dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    xq = torch.empty((L, cap, H), dtype=torch.uint8, device=dev)
+    sc, ld = mp.scale_tensor("packed", L * cap, H, g, dev, blocks=L)
+    mm = torch.empty(L, dtype=torch.int32, device=dev)
+    s2d = torch.empty((T, K), dtype=torch.int32, device=dev)
+    kept = int(((dd["topk_ids"] >= 0) & (dd["topk_ids"] < L)).sum())
+    live_tok = int((((dd["topk_ids"] >= 0) & (dd["topk_ids"] < L)).any(axis=1)).sum())
+
+    def dec():
+        assert mp.moe_dispatch_masked(x, H, T, None, H, ids, None, K, E, L, cap, g, "packed", xq, sc,
+                                      ld, mm, s2d, None, ws.buf, ws.nbytes, st) == 0
+    us = time_call(dec, flush)
+    nb = live_tok * H * 2 + T * K * 4 + kept * (H + 56) + L * 4 + T * K * 4
+    res["decode_masked_dispatch"] = entry(us, nb)
+    yslab = torch.randn((L * cap, H), device=dev).to(torch.bfloat16)
+    outd = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+
+    def decomb():
+        assert mp.moe_combine(yslab, H, L * cap, s2d, w, T, None, K, H, outd, st) == 0
+    us = time_call(decomb, flush)
+    res["decode_combine_from_slab"] = entry(us, kept * H * 2 + T * K * 8 + T * H * 2)
+
+    # MXFP8 sparse buffer: 112 live rows of 24576
+    dm = synth.mxfp8(0)
+    cm = dm["cfg"]
+    xb = torch.from_numpy(dm["x"].view(np.int16)).to(dev).view(torch.bfloat16)
+    nl = torch.tensor([cm["n_live"]], dtype=torch.int32, device=dev)
+    xqm = torch.empty((cm["T_cap"], cm["H"]), dtype=torch.uint8, device=dev)
+    scm = torch.empty((cm["T_cap"], cm["H"] // 32), dtype=torch.uint8, device=dev)
+
+    def mx():
+        assert mp.moe_quant_group(xb, cm["H"], cm["T_cap"], nl, cm["H"], 32, "u8", xqm, scm,
+                                  cm["H"] // 32, st) == 0
+    us = time_call(mx, flush)
+    res["mxfp8_live_quant"] = entry(us, cm["n_live"] * cm["H"] * 3 + cm["n_live"] * 224)
+    res["mxfp8_live_quant"]["capacity_rows"] = cm["T_cap"]
+
+    # requant
+    dr = synth.requant(0)
+    cr = dr["cfg"]
+    q = torch.from_numpy(dr["q"]).to(dev)
+    s = torch.from_numpy(dr["s_tok"]).to(dev)
+    qo = torch.empty_like(q)
+    S = torch.empty(1, dtype=torch.float32, device=dev)
+
+    def rq():
+        assert mp.fp8_requant_per_tensor(q, cr["H"], s, cr["T"], cr["H"], qo, S) == 0
+    us = time_call(rq, flush)
+    res["requant_per_tensor"] = entry(us, 2 * cr["T"] * cr["H"] + cr["T"] * 4 + 4)
+
+    # expand -> slab -> expand (fp8 + packed scales), 64 experts, 4096 rows
+    counts = synth.repack_counts(dr["rng"], cr["L"], cr["blocks"], cr["align"])
+    psum_l, prev = [], 0
+    for cnt in counts:
+        st0 = -(-prev // 128) * 128
+        psum_l.append(st0 + int(cnt))
+        prev = st0 + int(cnt)
+    R = cr["T"]
+    capr = int(-(-counts.max() // 128) * 128)
+    psum = torch.tensor(psum_l, dtype=torch.int32, device=dev)
+    G = cr["H"] // 128
+    esc, ld_es = mp.scale_tensor("packed", R, cr["H"], 128, dev)
+    slab = torch.empty((cr["L"] * capr, cr["H"]), dtype=torch.uint8, device=dev)
+    ssc, ld_ss = mp.scale_tensor("packed", cr["L"] * capr, cr["H"], 128, dev, blocks=cr["L"])
+    mmr = torch.empty(cr["L"], dtype=torch.int32, device=dev)
+    back = torch.empty_like(q)
+    mi = torch.empty(R, dtype=torch.int32, device=dev)
+    real = int(counts.sum())
+
+    def to_slab():
+        assert mp.moe_expand_to_slab(q, 1, cr["H"], R, esc, ld_es, psum, cr["L"], 128, capr, "packed",
+                                     128, slab, ssc, ld_ss, mmr, st) == 0
+
+    def from_slab():
+        assert mp.moe_expand_from_slab(slab, 1, cr["H"], ssc, ld_ss, psum, cr["L"], 128, capr,
+                                       "packed", 128, None, back, R, esc, ld_es, mi, st) == 0
+    nb = 2 * real * (cr["H"] + ((G + 3) // 4) * 4) + cr["L"] * 8
+    res["expand_to_slab"] = entry(time_call(to_slab, flush), nb)
+    res["slab_to_expand"] = entry(time_call(from_slab, flush), nb + R * 4)
+    torch.cuda.synchronize()
+    assert mp.moe_status_sync(st) == 0
+    return res
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    run_ours(args, rank, world, local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,309 @@
+// api.cu -- the C ABI of libmoeperm (include/moeperm.h): host-side argument
+// validation, workspace carving and kernel launches. No allocation, no
+// synchronisation (except moe_status_sync), no host <-> device traffic.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moeperm.h"
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace moeperm;
+
+namespace {
+
+constexpr int kMaxK = 32;
+constexpr int kMaxL = 1024;
+constexpr int64_t kMaxAssignments = int64_t(1) << 20;
+constexpr size_t kWsHeader = 256;  // ticket word, padded
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int num_sms_cached() {
+  static int cache[128] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 0;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+bool fmt_ok(int fmt, int g) {
+  if (g == 128) return fmt == MOE_SCALE_UE8M0_U8 || fmt == MOE_SCALE_UE8M0_PACKED ||
+                       fmt == MOE_SCALE_F32_POW2;
+  if (g == 32) return fmt == MOE_SCALE_UE8M0_U8;
+  return false;
+}
+
+// Leading-dimension rule of a scale buffer whose blocks hold `rows_per_block` rows.
+bool ld_ok(int fmt, int64_t ld, int64_t rows_per_block, int G) {
+  if (fmt == MOE_SCALE_UE8M0_PACKED) return ld >= rows_per_block && ld % 4 == 0 && ld > 0;
+  return ld >= G;
+}
+
+int64_t route_nchunks(int64_t A, int S) {
+  const int64_t per = 256 * (int64_t)S;
+  int64_t n = (A + per - 1) / per;
+  return n < 1 ? 1 : n;
+}
+
+moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+struct DispatchCommon {
+  const void* x; int64_t ldx; int32_t T; const int32_t* d_num_tokens; int32_t H;
+  const int32_t* ids; const float* w; int32_t K, E, L, g; int fmt;
+  void* xq; void* scales; int64_t ld_s; int32_t* src2dst; float* row_weights;
+  void* ws; size_t ws_bytes;
+};
+
+moe_status_t check_common(const DispatchCommon& c) {
+  if (c.T < 0 || c.H <= 0 || c.H % 16 || (c.g != 32 && c.g != 128) || c.H % c.g) return MOE_ERR_INVALID_ARG;
+  if (!fmt_ok(c.fmt, c.g)) return MOE_ERR_INVALID_ARG;
+  if (c.K < 1 || c.K > kMaxK || c.L < 1 || c.L > kMaxL || c.E < c.L) return MOE_ERR_INVALID_ARG;
+  if ((int64_t)c.T * c.K > kMaxAssignments) return MOE_ERR_INVALID_ARG;
+  if (c.T > 0) {
+    if (!c.x || !aligned16(c.x) || c.ldx < c.H || c.ldx % 8) return MOE_ERR_INVALID_ARG;
+    if (!c.ids || !c.src2dst) return MOE_ERR_INVALID_ARG;
+  }
+  if (!c.xq || !aligned16(c.xq) || !c.scales || !aligned16(c.scales)) return MOE_ERR_INVALID_ARG;
+  if (c.row_weights && !c.w) return MOE_ERR_INVALID_ARG;
+  if (!c.ws || !aligned16(c.ws) || c.ws_bytes < moe_workspace_bytes(c.T, c.K, c.L))
+    return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+moe_status_t run_dispatch(const DispatchCommon& c, int mode, int32_t block_e, int32_t cap,
+                          int32_t* m_indices, int64_t bound, int32_t* counts, int32_t* starts,
+                          int32_t* psum, int32_t* total, int32_t* masked_m, int32_t* d_status,
+                          cudaStream_t stream) {
+  const int sms = num_sms_cached();
+  if (sms <= 0) return MOE_ERR_CUDA;
+  const int64_t A = (int64_t)c.T * c.K;
+  const int S = route_plan_S(A);
+  const int64_t nchunks = route_nchunks(A, S);
+  unsigned int* ticket = reinterpret_cast<unsigned int*>(c.ws);
+  int32_t* table = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(c.ws) + kWsHeader);
+
+  RoutePlanArgs rp{};
+  rp.ids = c.ids; rp.d_num_tokens = c.d_num_tokens;
+  rp.T = c.T; rp.K = c.K; rp.L = c.L; rp.mode = mode; rp.block_e = block_e; rp.cap = cap;
+  rp.chunk = 256 * S; rp.nchunks = (int32_t)nchunks;
+  rp.lrank = c.src2dst; rp.table = table; rp.ticket = ticket;
+  rp.counts = counts; rp.starts = starts; rp.psum = psum; rp.total = total;
+  rp.masked_m = masked_m; rp.status = d_status;
+  cudaError_t err = launch_route_plan(rp, S, stream);
+  if (err != cudaSuccess) return MOE_ERR_CUDA;
+
+  ScatterArgs sa{};
+  sa.x = static_cast<const uint16_t*>(c.x); sa.ldx = c.ldx; sa.T = c.T;
+  sa.d_num_tokens = c.d_num_tokens; sa.H = c.H; sa.ids = c.ids; sa.w = c.w;
+  sa.K = c.K; sa.L = c.L; sa.mode = mode; sa.cap = cap; sa.chunk = rp.chunk; sa.table = table;
+  sa.xq = static_cast<uint8_t*>(c.xq); sa.scales = c.scales; sa.ld_s = c.ld_s;
+  sa.src2dst = c.src2dst; sa.row_weights = c.row_weights;
+  sa.m_indices = m_indices; sa.bound = bound; sa.starts = starts; sa.psum = psum;
+  sa.status = d_status;
+  return cuda_status(launch_quant_scatter(sa, c.g, c.fmt, sms, stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+int64_t moe_compact_bound(int64_t A, int32_t L, int32_t block_e) {
+  if (A < 0 || L < 1 || block_e < 1) return 0;
+  const int64_t n = A < L ? A : L;
+  return (int64_t)block_e * (n + (A - n) / block_e);
+}
+
+int32_t moe_should_use_masked(int32_t E, int32_t L) { return (E > L && L <= 32) ? 1 : 0; }
+
+size_t moe_scale_bytes(moe_scale_fmt_t fmt, int64_t rows, int32_t H, int32_t g) {
+  if (rows < 0 || H <= 0 || (g != 32 && g != 128) || H % g || !fmt_ok(fmt, g)) return 0;
+  const int64_t G = H / g;
+  if (fmt == MOE_SCALE_UE8M0_U8) return (size_t)(rows * G);
+  if (fmt == MOE_SCALE_F32_POW2) return (size_t)(rows * G * 4);
+  return (size_t)(((G + 3) / 4) * 4 * ((rows + 3) / 4 * 4));
+}
+
+size_t moe_workspace_bytes(int32_t T, int32_t K, int32_t L) {
+  if (T < 0 || K < 1 || L < 1) return 0;
+  const int64_t A = (int64_t)T * K;
+  const int64_t nchunks = route_nchunks(A, route_plan_S(A));
+  return kWsHeader + (size_t)nchunks * (size_t)L * sizeof(int32_t);
+}
+
+moe_status_t moe_dispatch_compact(
+    const void* x, int64_t ldx, int32_t T, const int32_t* d_num_tokens, int32_t H,
+    const int32_t* topk_ids, const float* topk_weights, int32_t K, int32_t E, int32_t L,
+    int32_t block_e, int32_t g, moe_scale_fmt_t fmt,
+    void* xq, void* scales, int64_t ld_s, int32_t* m_indices, int64_t bound,
+    int32_t* src2dst, int32_t* counts, int32_t* starts, int32_t* psum, int32_t* total,
+    float* row_weights, void* workspace, size_t workspace_bytes, int32_t* d_status,
+    moe_stream_t stream) {
+  DispatchCommon c{x, ldx, T, d_num_tokens, H, topk_ids, topk_weights, K, E, L, g, (int)fmt,
+                   xq, scales, ld_s, src2dst, row_weights, workspace, workspace_bytes};
+  moe_status_t st = check_common(c);
+  if (st != MOE_OK) return st;
+  if (block_e < 1) return MOE_ERR_INVALID_ARG;
+  const int64_t need = moe_compact_bound((int64_t)T * K, L, block_e);
+  if (bound < need || bound >= (int64_t(1) << 31)) return MOE_ERR_INVALID_ARG;
+  if (!m_indices || !counts || !starts || !psum || !total) return MOE_ERR_INVALID_ARG;
+  if (!ld_ok(fmt, ld_s, bound, H / g)) return MOE_ERR_INVALID_ARG;
+  return run_dispatch(c, kModeCompact, block_e, 0, m_indices, bound, counts, starts, psum,
+                      total, nullptr, d_status, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_dispatch_masked(
+    const void* x, int64_t ldx, int32_t T, const int32_t* d_num_tokens, int32_t H,
+    const int32_t* topk_ids, const float* topk_weights, int32_t K, int32_t E, int32_t L,
+    int32_t cap, int32_t g, moe_scale_fmt_t fmt,
+    void* xq, void* scales, int64_t ld_s, int32_t* masked_m, int32_t* src2dst,
+    float* row_weights, void* workspace, size_t workspace_bytes, int32_t* d_status,
+    moe_stream_t stream) {
+  DispatchCommon c{x, ldx, T, d_num_tokens, H, topk_ids, topk_weights, K, E, L, g, (int)fmt,
+                   xq, scales, ld_s, src2dst, row_weights, workspace, workspace_bytes};
+  moe_status_t st = check_common(c);
+  if (st != MOE_OK) return st;
+  if (cap < 1 || (int64_t)L * cap >= (int64_t(1) << 31)) return MOE_ERR_INVALID_ARG;
+  if (!masked_m) return MOE_ERR_INVALID_ARG;
+  if (!ld_ok(fmt, ld_s, cap, H / g)) return MOE_ERR_INVALID_ARG;
+  return run_dispatch(c, kModeMasked, 1, cap, nullptr, 0, nullptr, nullptr, nullptr, nullptr,
+                      masked_m, d_status, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_quant_group(const void* x, int64_t ldx, int32_t T_cap, const int32_t* d_num_live,
+                             int32_t H, int32_t g, moe_scale_fmt_t fmt, void* xq, void* scales,
+                             int64_t ld_s, int32_t* d_status, moe_stream_t stream) {
+  if (T_cap < 0 || H <= 0 || H % 16 || (g != 32 && g != 128) || H % g || !fmt_ok(fmt, g))
+    return MOE_ERR_INVALID_ARG;
+  if (T_cap == 0) return MOE_OK;
+  if (!x || !aligned16(x) || ldx < H || ldx % 8) return MOE_ERR_INVALID_ARG;
+  if (!xq || !aligned16(xq) || !scales || !aligned16(scales)) return MOE_ERR_INVALID_ARG;
+  if (!ld_ok(fmt, ld_s, T_cap, H / g)) return MOE_ERR_INVALID_ARG;
+  const int sms = num_sms_cached();
+  if (sms <= 0) return MOE_ERR_CUDA;
+  ScatterArgs sa{};
+  sa.x = static_cast<const uint16_t*>(x); sa.ldx = ldx; sa.T = T_cap; sa.d_num_tokens = d_num_live;
+  sa.H = H; sa.K = 1; sa.L = 1; sa.mode = kModeIdentity; sa.cap = 0; sa.chunk = 1;
+  sa.xq = static_cast<uint8_t*>(xq); sa.scales = scales; sa.ld_s = ld_s; sa.status = d_status;
+  return cuda_status(launch_quant_scatter(sa, g, (int)fmt, sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_combine(const void* y, int64_t ldy, int64_t R, const int32_t* src2dst,
+                         const float* w, int32_t T, const int32_t* d_num_tokens, int32_t K,
+                         int32_t H, void* out, int32_t* d_status, moe_stream_t stream) {
+  if (T < 0 || K < 1 || K > kMaxK || H <= 0 || H % 8 || R < 0) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!src2dst || !out || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+  if (R > 0 && (!y || !aligned16(y) || ldy < H || ldy % 8)) return MOE_ERR_INVALID_ARG;
+  const int sms = num_sms_cached();
+  if (sms <= 0) return MOE_ERR_CUDA;
+  CombineArgs ca{};
+  ca.y = static_cast<const uint16_t*>(y); ca.ldy = ldy; ca.R = R; ca.src2dst = src2dst; ca.w = w;
+  ca.T = T; ca.d_num_tokens = d_num_tokens; ca.K = K; ca.H = H;
+  ca.out = static_cast<uint16_t*>(out); ca.status = d_status;
+  return cuda_status(launch_combine(ca, sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+static moe_status_t repack_common(int to_slab, const void* src, void* dst, int32_t elem_bytes,
+                                  int32_t H, int64_t R, const void* src_scales, int64_t ld_src,
+                                  void* dst_scales, int64_t ld_dst, const int32_t* psum, int32_t L,
+                                  int32_t align, int32_t cap, moe_scale_fmt_t fmt, int32_t g,
+                                  const float* row_weights, int32_t* masked_m, int32_t* m_indices,
+                                  int32_t* d_status, cudaStream_t stream) {
+  if ((elem_bytes != 1 && elem_bytes != 2) || H <= 0 || H % 16 || R < 0) return MOE_ERR_INVALID_ARG;
+  if (L < 1 || L > kMaxL || align < 1 || cap < 1 || (int64_t)L * cap >= (int64_t(1) << 31))
+    return MOE_ERR_INVALID_ARG;
+  if (R >= (int64_t(1) << 31) || !psum) return MOE_ERR_INVALID_ARG;
+  if (!src || !dst || !aligned16(src) || !aligned16(dst)) return MOE_ERR_INVALID_ARG;
+  if ((src_scales == nullptr) != (dst_scales == nullptr)) return MOE_ERR_INVALID_ARG;
+  int G = 0;
+  if (src_scales) {
+    if (elem_bytes != 1 || (g != 32 && g != 128) || H % g || !fmt_ok(fmt, g)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(src_scales) || !aligned16(dst_scales)) return MOE_ERR_INVALID_ARG;
+    G = H / g;
+    const int64_t ld_exp = to_slab ? ld_src : ld_dst;
+    const int64_t ld_slab = to_slab ? ld_dst : ld_src;
+    if (!ld_ok(fmt, ld_exp, R, G) || !ld_ok(fmt, ld_slab, cap, G)) return MOE_ERR_INVALID_ARG;
+  }
+  if (row_weights && elem_bytes != 2) return MOE_ERR_INVALID_ARG;
+  const int sms = num_sms_cached();
+  if (sms <= 0) return MOE_ERR_CUDA;
+  RepackArgs ra{};
+  ra.to_slab = to_slab; ra.src = static_cast<const uint8_t*>(src); ra.dst = static_cast<uint8_t*>(dst);
+  ra.elem_bytes = elem_bytes; ra.H = H; ra.R = R;
+  ra.src_scales = src_scales; ra.ld_src_s = ld_src; ra.dst_scales = dst_scales; ra.ld_dst_s = ld_dst;
+  ra.psum = psum; ra.L = L; ra.align = align; ra.cap = cap; ra.fmt = (int)fmt; ra.G = G;
+  ra.row_weights = row_weights; ra.masked_m = masked_m; ra.m_indices = m_indices; ra.status = d_status;
+  return cuda_status(launch_repack(ra, sms, stream));
+}
+
+moe_status_t moe_expand_to_slab(const void* exp, int32_t elem_bytes, int32_t H, int64_t R,
+                                const void* exp_scales, int64_t ld_es, const int32_t* psum,
+                                int32_t L, int32_t align, int32_t cap, moe_scale_fmt_t fmt,
+                                int32_t g, void* slab, void* slab_scales, int64_t ld_ss,
+                                int32_t* masked_m, int32_t* d_status, moe_stream_t stream) {
+  if (!masked_m) return MOE_ERR_INVALID_ARG;
+  return repack_common(1, exp, slab, elem_bytes, H, R, exp_scales, ld_es, slab_scales, ld_ss,
+                       psum, L, align, cap, fmt, g, nullptr, masked_m, nullptr, d_status,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_expand_from_slab(const void* slab, int32_t elem_bytes, int32_t H,
+                                  const void* slab_scales, int64_t ld_ss, const int32_t* psum,
+                                  int32_t L, int32_t align, int32_t cap, moe_scale_fmt_t fmt,
+                                  int32_t g, const float* row_weights, void* exp, int64_t R,
+                                  void* exp_scales, int64_t ld_es, int32_t* m_indices,
+                                  int32_t* d_status, moe_stream_t stream) {
+  return repack_common(0, slab, exp, elem_bytes, H, R, slab_scales, ld_ss, exp_scales, ld_es,
+                       psum, L, align, cap, fmt, g, row_weights, nullptr, m_indices, d_status,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t fp8_requant_per_tensor(const void* q, int64_t ldq, const float* s_tok, int32_t T,
+                                    int32_t H, void* q_out, float* d_scale_out,
+                                    moe_stream_t stream) {
+  if (T < 0 || H <= 0 || H % 16 || !d_scale_out) return MOE_ERR_INVALID_ARG;
+  if (T > 0) {
+    if (!q || !aligned16(q) || ldq < H || ldq % 16 || !s_tok) return MOE_ERR_INVALID_ARG;
+    if (!q_out || !aligned16(q_out)) return MOE_ERR_INVALID_ARG;
+  }
+  const int sms = num_sms_cached();
+  if (sms <= 0) return MOE_ERR_CUDA;
+  RequantArgs ra{};
+  ra.q = static_cast<const uint8_t*>(q); ra.ldq = ldq; ra.s_tok = s_tok; ra.T = T; ra.H = H;
+  ra.q_out = static_cast<uint8_t*>(q_out); ra.scale_out = d_scale_out;
+  return cuda_status(launch_requant(ra, sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_status_sync(const int32_t* d_status, moe_stream_t stream) {
+  if (!d_status) return MOE_ERR_INVALID_ARG;
+  int32_t v = 0;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&v, d_status, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (v & MOE_STATUS_OVERFLOW) return MOE_ERR_OVERFLOW;
+  if (v & MOE_STATUS_LIVE_OVERFLOW) return MOE_ERR_LIVE_OVERFLOW;
+  if (v & MOE_STATUS_BAD_LAYOUT) return MOE_ERR_BAD_LAYOUT;
+  return MOE_OK;
+}
+
+const char* moe_status_string(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument (rejected before launch)";
+    case MOE_ERR_OVERFLOW: return "an expert received more rows than its slab capacity";
+    case MOE_ERR_LIVE_OVERFLOW: return "live-row count larger than the buffer";
+    case MOE_ERR_BAD_LAYOUT: return "prefix sums or row indices inconsistent with the buffers";
+    case MOE_ERR_CUDA: return "CUDA runtime error";
+  }
+  return "unknown status";
+}
+
+const char* moe_version(void) { return "moeperm 0.1 sm_103a"; }
+
+}  // extern "C"

@@ -1,0 +1,139 @@
+// common.cuh -- device helpers shared by the sm_103a kernels of libmoeperm.
+//
+// Number formats:
+//   bf16 values travel as raw 16-bit words, two per 32-bit register (element 0
+//   in the low half), so the absolute maximum of a group is an unsigned 16-bit
+//   max of sign-cleared words (for finite values the bit order is the value
+//   order) -- no float compare is needed.
+//   e4m3 (OCP E4M3) conversions use the hardware pair converts
+//   cvt.rn.satfinite.e4m3x2.f32 (round to nearest even, saturating to +-448)
+//   and cvt.rn.f16x2.e4m3x2 (exact widening).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moeperm {
+
+// Device status bits (same values as MOE_STATUS_* in the public header).
+constexpr int kStOverflow = 0x1;
+constexpr int kStLiveOverflow = 0x2;
+constexpr int kStBadLayout = 0x4;
+
+// Scale layouts (same values as moe_scale_fmt_t).
+constexpr int kFmtU8 = 0;
+constexpr int kFmtPacked = 1;
+constexpr int kFmtF32 = 2;
+
+// Route-plan modes.
+constexpr int kModeCompact = 0;
+constexpr int kModeMasked = 1;
+constexpr int kModeIdentity = 2;  // row t -> row t (live-row quantisation)
+
+__device__ __forceinline__ void set_status(int32_t* status, int bits) {
+  if (status != nullptr) atomicOr(status, bits);
+}
+
+// Live-row count read on the device: min(*d_n, cap) (and >= 0); flags n > cap.
+__device__ __forceinline__ int live_count(const int32_t* d_n, int cap, int32_t* status,
+                                          bool report) {
+  if (d_n == nullptr) return cap;
+  int n = __ldg(d_n);
+  if (n > cap) {
+    if (report) set_status(status, kStLiveOverflow);
+    n = cap;
+  }
+  return n < 0 ? 0 : n;
+}
+
+// ---------------------------------------------------------------------------
+// bf16 helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// max |x| over the 16 bf16 values of two 16-byte vectors, as a bf16 bit pattern
+// in the low half of the result.
+__device__ __forceinline__ uint32_t amax16_bf16(const uint4& a, const uint4& b) {
+  const uint32_t m = 0x7FFF7FFFu;
+  uint32_t r = __vmaxu2(__vmaxu2(a.x & m, a.y & m), __vmaxu2(a.z & m, a.w & m));
+  r = __vmaxu2(r, __vmaxu2(__vmaxu2(b.x & m, b.y & m), __vmaxu2(b.z & m, b.w & m)));
+  return max(r & 0xFFFFu, r >> 16);
+}
+
+// fp32 -> bf16 (round to nearest even) pair pack, element `lo` in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// ---------------------------------------------------------------------------
+// e4m3 helpers
+// ---------------------------------------------------------------------------
+
+// Two floats -> two e4m3 bytes (RNE, satfinite); `lo` lands in the low byte.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return (uint32_t)r;
+}
+
+// Two e4m3 bytes (low byte first) -> two floats, exactly (e4m3 -> f16 -> f32).
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two_bytes) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)two_bytes));
+  float2 f;
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+      : "=f"(f.x), "=f"(f.y)
+      : "r"(h2));
+  return f;
+}
+
+// Power-of-two group exponent: the smallest integer e with 448 * 2^e >= a,
+// a = max(amax, 1e-10). With a = 1.m * 2^E (a normal float): 448 = 1.75 * 2^8,
+// so e = E - 8 when 1.m <= 1.75 and E - 7 otherwise. Exact, no division.
+__device__ __forceinline__ int group_exponent(float amax) {
+  const float a = fmaxf(amax, 1e-10f);
+  const uint32_t bits = __float_as_uint(a);
+  const int E = (int)(bits >> 23) - 127;
+  const uint32_t mant = bits & 0x7FFFFFu;
+  int e = E - 8 + (mant > 0x600000u ? 1 : 0);
+  return min(max(e, -127), 127);
+}
+
+// 2^-e as a float (e in [-126, 126]).
+__device__ __forceinline__ float exp2_neg(int e) {
+  return __uint_as_float((uint32_t)(127 - e) << 23);
+}
+
+// Quantise 8 bf16 values (one 16-byte vector) by 2^-e into 8 e4m3 bytes.
+__device__ __forceinline__ uint2 quant8(const uint4& v, float inv) {
+  uint2 r;
+  r.x = cvt_e4m3x2(__fmul_rn(bf16_lo(v.x), inv), __fmul_rn(bf16_hi(v.x), inv)) |
+        (cvt_e4m3x2(__fmul_rn(bf16_lo(v.y), inv), __fmul_rn(bf16_hi(v.y), inv)) << 16);
+  r.y = cvt_e4m3x2(__fmul_rn(bf16_lo(v.z), inv), __fmul_rn(bf16_hi(v.z), inv)) |
+        (cvt_e4m3x2(__fmul_rn(bf16_lo(v.w), inv), __fmul_rn(bf16_hi(v.w), inv)) << 16);
+  return r;
+}
+
+// ---------------------------------------------------------------------------
+// Memory helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
+  uint4 r;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ void st_v4(void* p, const uint4& v) {
+  asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+__device__ __forceinline__ int64_t align_up64(int64_t c, int64_t b) { return (c + b - 1) / b * b; }
+
+}  // namespace moeperm

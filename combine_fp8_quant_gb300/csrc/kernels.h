@@ -1,0 +1,119 @@
+// kernels.h -- internal launch interface between the C ABI (api.cu) and the
+// kernel translation units. Not installed; the public interface is
+// include/moeperm.h.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moeperm {
+
+// ---------------------------------------------------------------------------
+// Route plan: per-chunk expert histograms, stable in-chunk ranks, and (in the
+// last chunk to finish) the per-expert totals, segment starts and the table of
+// per-chunk row bases.
+// ---------------------------------------------------------------------------
+struct RoutePlanArgs {
+  const int32_t* ids;          // [T, K]
+  const int32_t* d_num_tokens; // optional live tokens
+  int32_t T, K, L;
+  int32_t mode;                // kModeCompact / kModeMasked
+  int32_t block_e, cap;
+  int32_t chunk;               // assignments per chunk (= 256 * S)
+  int32_t nchunks;
+  int32_t* lrank;              // [T*K] out: stable rank inside the chunk, -1 dropped
+  int32_t* table;              // [nchunks, L] workspace: chunk histogram -> row base
+  unsigned int* ticket;        // workspace word, zero between calls
+  int32_t* counts;             // [L] compact (may be null for masked)
+  int32_t* starts;             // [L] compact
+  int32_t* psum;               // [L] compact
+  int32_t* total;              // [1] compact
+  int32_t* masked_m;           // [L] masked
+  int32_t* status;
+};
+int route_plan_S(int64_t A);                        // assignments per lane per chunk
+cudaError_t launch_route_plan(const RoutePlanArgs& a, int S, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// Quantise + scatter (dispatch) / quantise live rows (identity mode).
+// ---------------------------------------------------------------------------
+struct ScatterArgs {
+  const uint16_t* x;
+  int64_t ldx;
+  int32_t T;
+  const int32_t* d_num_tokens;
+  int32_t H;
+  const int32_t* ids;
+  const float* w;
+  int32_t K, L;
+  int32_t mode;
+  int32_t cap;
+  int32_t chunk;
+  const int32_t* table;
+  uint8_t* xq;
+  void* scales;
+  int64_t ld_s;
+  int32_t* src2dst;            // in: chunk rank, out: final row (-1 dropped)
+  float* row_weights;
+  int32_t* m_indices;          // compact: [bound]
+  int64_t bound;
+  const int32_t* starts;       // compact: route-plan outputs used by the m_indices fill
+  const int32_t* psum;
+  int32_t* status;
+};
+cudaError_t launch_quant_scatter(const ScatterArgs& a, int g, int fmt, int num_sms,
+                                 cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// Combine
+// ---------------------------------------------------------------------------
+struct CombineArgs {
+  const uint16_t* y;
+  int64_t ldy;
+  int64_t R;
+  const int32_t* src2dst;
+  const float* w;
+  int32_t T;
+  const int32_t* d_num_tokens;
+  int32_t K, H;
+  uint16_t* out;
+  int32_t* status;
+};
+cudaError_t launch_combine(const CombineArgs& a, int num_sms, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// Expanded <-> slab repack
+// ---------------------------------------------------------------------------
+struct RepackArgs {
+  int32_t to_slab;             // 1: expanded -> slab, 0: slab -> expanded
+  const uint8_t* src;
+  uint8_t* dst;
+  int32_t elem_bytes, H;
+  int64_t R;                   // expanded rows
+  const void* src_scales;
+  int64_t ld_src_s;
+  void* dst_scales;
+  int64_t ld_dst_s;
+  const int32_t* psum;
+  int32_t L, align, cap, fmt, G;
+  const float* row_weights;    // slab -> expanded, bf16 only
+  int32_t* masked_m;           // expanded -> slab
+  int32_t* m_indices;          // slab -> expanded, optional [R]
+  int32_t* status;
+};
+cudaError_t launch_repack(const RepackArgs& a, int num_sms, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// Per-token -> per-tensor requant
+// ---------------------------------------------------------------------------
+struct RequantArgs {
+  const uint8_t* q;
+  int64_t ldq;
+  const float* s_tok;
+  int32_t T, H;
+  uint8_t* q_out;
+  float* scale_out;
+};
+cudaError_t launch_requant(const RequantArgs& a, int num_sms, cudaStream_t s);
+
+}  // namespace moeperm

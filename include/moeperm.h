@@ -1,0 +1,315 @@
+/*
+ * moeperm.h -- C ABI of libmoeperm.so: the single-GPU MoE token permute,
+ * FP8 group quantisation, combine and requantisation path, written for
+ * GB300 (sm_103a).
+ *
+ * Sources (SGLang pull-request digests, cited by page title and section):
+ *   [P1] "PR #33128 DeepGEMM standard MoE dispatch: compact layout and UE8M0
+ *        requant" -- 实现拆解 (implementation) items 2-4; 关键源码片段 (code
+ *        excerpts) _should_use_masked_standard_layout, _get_compact_all_tokens,
+ *        _fwd_kernel_ep_scatter_1; 风险与影响 item 2 (src2dst, post-permute).
+ *   [P2] "PR #14162 W4AFP8 DeepEP low-latency FP8 dispatch" -- 实现拆解 items
+ *        1-2 (fp8_per_token_to_per_tensor_quant); 评论区精华 (review).
+ *   [P3] "PR #29525 DeepEPv2 ElasticBuffer MoE A2A backend" -- 实现拆解 items
+ *        3-4 (expand_to_masked_slab, masked_slab_to_expand, 128-aligned psum,
+ *        fixed worker pool, stride-aware packed UE8M0 scales); 关键源码片段
+ *        _build_layout / _check_expand_roundtrip; 评论区精华 item 1 (masked
+ *        tail), 风险与影响 item 1 (overflow must fail fast).
+ *   [P4] "PR #36119 MXFP8 MoRI dispatch" -- 功能与动机 (quantise live rows
+ *        only), 实现拆解 items 1 and 4 (group 32, e8m0, 224 scales at 7168,
+ *        empty batch).
+ *
+ * General contract (every data call):
+ *   - All tensor arguments are DEVICE pointers owned by the caller. The library
+ *     never allocates, frees or synchronises (except moe_status_sync).
+ *   - Every data call enqueues its kernels on `stream` and returns without
+ *     waiting. The grid of every launch depends only on scalar arguments and
+ *     the device's SM count, never on routing contents or device-side counts,
+ *     so every call can be captured in a CUDA graph and replayed with new
+ *     contents of the same shapes.
+ *   - Argument errors (null required pointer, misalignment, unsupported
+ *     sizes / format / group pairs, a workspace that is too small) return
+ *     MOE_ERR_INVALID_ARG before anything is launched.
+ *   - Data-dependent errors (an expert above its slab capacity, a live-row
+ *     count above the buffer, inconsistent prefix sums, an out-of-range row
+ *     index) never cause an out-of-bounds access: the kernel writes only
+ *     in-bounds rows and ORs a MOE_STATUS_* bit into the caller's device word
+ *     `d_status`. The caller clears that word; bits accumulate across calls
+ *     until then. moe_status_sync() turns the word into a moe_status_t.
+ *   - Output rows the definition does not name (padding rows, slab rows past
+ *     an expert's count, rows of non-live tokens) are NOT written, as with an
+ *     uninitialised buffer [P1 实现拆解 item 4]. The only exception is
+ *     m_indices, which is written over its whole length.
+ *   - A launch failure returns MOE_ERR_CUDA (cudaGetLastError is consumed).
+ *   - bf16 tensors are raw 16-bit bfloat16 values, e4m3 tensors raw OCP E4M3
+ *     bytes. Row offsets are computed in 64-bit.
+ *   - Quantisation [P1 实现拆解 item 3, P4]: for each group of g consecutive
+ *     elements, e = ceil(log2(max(amax, 1e-10) / 448)) (the smallest e with
+ *     448 * 2^e >= max(amax, 1e-10)), the stored scale byte is e + 127 and each
+ *     element is RNE_e4m3(x * 2^-e). Inputs are finite.
+ */
+#ifndef MOEPERM_H
+#define MOEPERM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,   /* rejected on the host, nothing launched */
+  MOE_ERR_OVERFLOW = 2,      /* an expert received more rows than its slab capacity */
+  MOE_ERR_LIVE_OVERFLOW = 3, /* device live-row count larger than the buffer's rows */
+  MOE_ERR_BAD_LAYOUT = 4,    /* prefix sums / row indices inconsistent with the buffers */
+  MOE_ERR_CUDA = 5           /* a CUDA runtime call or launch failed */
+} moe_status_t;
+
+/* Bits ORed into the caller's device status word. */
+#define MOE_STATUS_OVERFLOW 0x1
+#define MOE_STATUS_LIVE_OVERFLOW 0x2
+#define MOE_STATUS_BAD_LAYOUT 0x4
+
+/*
+ * Scale layouts ([P3 实现拆解 items 3-4: Blackwell column-major packed UE8M0 vs
+ * Hopper row-major fp32]; [P4 实现拆解 item 1: one e8m0 byte per group]).
+ * G = H / g groups per row, G4 = ceil(G / 4).
+ *
+ *  MOE_SCALE_UE8M0_U8     uint8 [rows, ld_s], ld_s >= G; byte (r, j) at r*ld_s + j
+ *                         holds e + 127. Bytes j >= G of a row are not written.
+ *  MOE_SCALE_UE8M0_PACKED int32 words, column-major per block: rows are split
+ *                         into blocks (the whole buffer for a compact or expanded
+ *                         layout; one block of `cap` rows per expert for a slab).
+ *                         Word (r, w) of block b is at b*G4*ld_s + w*ld_s + r, with
+ *                         ld_s >= rows-per-block and ld_s % 4 == 0 (16-byte
+ *                         columns). Word w holds groups 4w..4w+3, group 4w in the
+ *                         least significant byte; bytes past group G-1 are 0.
+ *  MOE_SCALE_F32_POW2     float [rows, ld_s], ld_s >= G; element (r, j) = 2^e.
+ *
+ * Supported (format, group) pairs: g = 128 with any of the three; g = 32 with
+ * MOE_SCALE_UE8M0_U8 (the MXFP8 layout).
+ */
+typedef enum {
+  MOE_SCALE_UE8M0_U8 = 0,
+  MOE_SCALE_UE8M0_PACKED = 1,
+  MOE_SCALE_F32_POW2 = 2
+} moe_scale_fmt_t;
+
+/* ------------------------------------------------------------------ */
+/* Host helpers (no GPU work)                                          */
+/* ------------------------------------------------------------------ */
+
+/* [P1 code excerpt _get_compact_all_tokens] Static row count of the compact
+ * layout for A = T*K assignments over L local experts with segments padded to
+ * block_e rows: block_e * (n + (A - n) / block_e), n = min(A, L). Every
+ * routing fits. Returns 0 for A < 0, L < 1 or block_e < 1. */
+int64_t moe_compact_bound(int64_t A, int32_t L, int32_t block_e);
+
+/* [P1 code excerpt _should_use_masked_standard_layout] 1 iff E > L and L <= 32
+ * (masked slab layout), else 0 (compact layout). */
+int32_t moe_should_use_masked(int32_t E, int32_t L);
+
+/* Bytes of a scale buffer of `fmt` for `rows` rows of H elements in groups of g,
+ * with the tightest leading dimension (U8: G, F32: G floats, PACKED: rows
+ * rounded up to 4, G4 words per row). 0 on an invalid combination. */
+size_t moe_scale_bytes(moe_scale_fmt_t fmt, int64_t rows, int32_t H, int32_t g);
+
+/* Bytes of device workspace the dispatch calls need for T tokens, K slots and L
+ * local experts. The workspace must be zero-filled once before its first use;
+ * every dispatch call leaves it ready for the next (its ticket word returns to
+ * zero). One workspace must not be used by two calls that can run at once. */
+size_t moe_workspace_bytes(int32_t T, int32_t K, int32_t L);
+
+/* ------------------------------------------------------------------ */
+/* Dispatch: route + quantise + scatter                                */
+/* ------------------------------------------------------------------ */
+
+/*
+ * moe_dispatch_compact -- [P1 实现拆解 items 2-4, code excerpts
+ * _get_compact_all_tokens and _fwd_kernel_ep_scatter_1; P3 实现拆解 item 4 and
+ * _build_layout (the same 128-aligned psum layout)].
+ *
+ * Inputs
+ *   x [T, ldx] bf16              activations, rows 16-byte aligned (ldx % 8 == 0)
+ *   T                            token rows of x / topk_ids / topk_weights
+ *   d_num_tokens (optional)      device int32: live tokens n <= T; tokens >= n are
+ *                                not routed and their x / ids / weights rows are
+ *                                never read. NULL means n = T. n > T is clamped
+ *                                and sets MOE_STATUS_LIVE_OVERFLOW.
+ *   H                            hidden size, H % 16 == 0 and H % g == 0
+ *   topk_ids [T, K] int32        expert id per slot; ids outside [0, L) are not
+ *                                local and are dropped (src2dst = -1)
+ *   topk_weights [T, K] f32      (optional) copied to row_weights
+ *   K (1..32), E (>= L), L (1..1024) experts in the model / local experts
+ *   block_e                      segment alignment (>= 1), 128 in the sources
+ *   g, fmt                       group size and scale layout (pairs above)
+ * Outputs (rows of the compact layout, bound = moe_compact_bound(T*K, L, block_e);
+ * the caller's buffers must hold at least `bound` rows)
+ *   xq [bound, H] e4m3           row r = quantised token of the slot that owns r
+ *   scales (fmt, ld_s)           scales of the same rows
+ *   m_indices [bound] int32      expert id on valid rows, -1 on padding rows and on
+ *                                the tail [total, bound) -- written in full
+ *   src2dst [T, K] int32         row of each slot, -1 if dropped (all T rows written)
+ *   counts, starts, psum [L]     rows per expert, segment start (a multiple of
+ *                                block_e), start + count
+ *   total [1]                    sum over experts of count rounded up to block_e
+ *   row_weights [bound] f32      (optional) topk weight of the slot owning each row
+ * Rows of an expert follow ascending t*K + k (a deterministic, stable order).
+ * The segment of expert e is [starts[e], starts[e] + align(counts[e])); starts
+ * are the exclusive prefix sums of the aligned counts.
+ * Workspace: moe_workspace_bytes(T, K, L) bytes, zero-filled before first use.
+ * Launches: 2 (route plan; quantise + scatter + m_indices), fixed grids.
+ */
+moe_status_t moe_dispatch_compact(
+    const void* x, int64_t ldx, int32_t T, const int32_t* d_num_tokens, int32_t H,
+    const int32_t* topk_ids, const float* topk_weights, int32_t K, int32_t E, int32_t L,
+    int32_t block_e, int32_t g, moe_scale_fmt_t fmt,
+    void* xq, void* scales, int64_t ld_s, int32_t* m_indices, int64_t bound,
+    int32_t* src2dst, int32_t* counts, int32_t* starts, int32_t* psum, int32_t* total,
+    float* row_weights, void* workspace, size_t workspace_bytes, int32_t* d_status,
+    moe_stream_t stream);
+
+/*
+ * moe_dispatch_masked -- [P1 实现拆解 item 2-3 (masked path,
+ * moe_ep_deepgemm_preprocess), P3 关键源码片段 (masked slab [E_local, max_m,
+ * hidden], masked_m = real counts)].
+ *
+ * Same inputs as moe_dispatch_compact, plus
+ *   cap                          slab rows per local expert (max_m), >= 1
+ * Outputs
+ *   xq [L, cap, H] e4m3          slab row (e, j) = j-th slot routed to e
+ *   scales (fmt, ld_s)           for PACKED one block of `cap` rows per expert
+ *   masked_m [L] int32           min(count, cap)
+ *   src2dst [T, K] int32         e*cap + j, or -1 if dropped or past capacity
+ *   row_weights [L*cap] f32      (optional)
+ * An expert with more than cap slots sets MOE_STATUS_OVERFLOW; its slots past
+ * cap are not written (fail fast, never truncate silently: [P3 风险与影响 1]).
+ * Workspace and launches as moe_dispatch_compact.
+ */
+moe_status_t moe_dispatch_masked(
+    const void* x, int64_t ldx, int32_t T, const int32_t* d_num_tokens, int32_t H,
+    const int32_t* topk_ids, const float* topk_weights, int32_t K, int32_t E, int32_t L,
+    int32_t cap, int32_t g, moe_scale_fmt_t fmt,
+    void* xq, void* scales, int64_t ld_s, int32_t* masked_m, int32_t* src2dst,
+    float* row_weights, void* workspace, size_t workspace_bytes, int32_t* d_status,
+    moe_stream_t stream);
+
+/*
+ * moe_quant_group -- [P4 功能与动机 and 实现拆解 item 1: quantise on the send side
+ * over the live rows only]. Quantises rows [0, n) of x, n = *d_num_live (or
+ * T_cap when NULL; n > T_cap is clamped and sets MOE_STATUS_LIVE_OVERFLOW).
+ * Rows >= n of x are never read and rows >= n of xq / scales never written; the
+ * launch does not depend on n.
+ *   x [T_cap, ldx] bf16, xq [T_cap, H] e4m3, scales (fmt, ld_s) over T_cap rows.
+ * Launches: 1.
+ */
+moe_status_t moe_quant_group(
+    const void* x, int64_t ldx, int32_t T_cap, const int32_t* d_num_live, int32_t H,
+    int32_t g, moe_scale_fmt_t fmt, void* xq, void* scales, int64_t ld_s,
+    int32_t* d_status, moe_stream_t stream);
+
+/* ------------------------------------------------------------------ */
+/* Combine                                                             */
+/* ------------------------------------------------------------------ */
+
+/*
+ * moe_combine -- [P1 风险与影响 item 2, post_permute_deep_gemm_to_standard via
+ * src2dst]. out[t, :] = bf16_RNE( sum over k with src2dst[t,k] >= 0 of
+ * w[t,k] * y[src2dst[t,k], :] ), accumulated in fp32 with one fused
+ * multiply-add per slot in ascending k, starting from +0. A token with every
+ * slot dropped gets zeros.
+ *   y [R, ldy] bf16               expert outputs in any row layout (compact rows,
+ *                                 slab rows e*cap + j, expanded rows); ldy % 8 == 0
+ *   src2dst [T, K] int32          rows of y; an index >= R sets MOE_STATUS_BAD_LAYOUT
+ *                                 and that slot is skipped
+ *   w [T, K] f32                  (optional; NULL means every weight is 1)
+ *   d_num_tokens (optional)       live tokens n; rows t >= n of out are not written
+ *   out [T, H] bf16               H % 8 == 0
+ * Launches: 1.
+ */
+moe_status_t moe_combine(
+    const void* y, int64_t ldy, int64_t R, const int32_t* src2dst, const float* w,
+    int32_t T, const int32_t* d_num_tokens, int32_t K, int32_t H, void* out,
+    int32_t* d_status, moe_stream_t stream);
+
+/* ------------------------------------------------------------------ */
+/* Expanded (psum) layout <-> masked slab repack                        */
+/* ------------------------------------------------------------------ */
+
+/*
+ * moe_expand_to_slab -- [P3 实现拆解 item 3 expand_to_masked_slab; 关键源码片段
+ * _build_layout]. In the expanded layout expert e owns rows
+ * [align(psum[e-1]), psum[e]) of exp (psum[-1] = 0, `align` >= 1). Copies row j
+ * of expert e to slab row (e, j) for j < min(count_e, cap), with its scales when
+ * exp_scales / slab_scales are given (e4m3 payload only), and writes
+ * masked_m[e] = min(count_e, cap). count_e > cap sets MOE_STATUS_OVERFLOW;
+ * psum inconsistent with R sets MOE_STATUS_BAD_LAYOUT (nothing is read past R).
+ *   exp [R, H] elements of elem_bytes (1 = e4m3, 2 = bf16); exp_scales (fmt, ld_es)
+ *   slab [L, cap, H]; slab_scales (fmt, ld_ss; PACKED: one block of cap rows per
+ *   expert)
+ * Launches: 1 (fixed grid over the R expanded rows).
+ */
+moe_status_t moe_expand_to_slab(
+    const void* exp, int32_t elem_bytes, int32_t H, int64_t R, const void* exp_scales,
+    int64_t ld_es, const int32_t* psum, int32_t L, int32_t align, int32_t cap,
+    moe_scale_fmt_t fmt, int32_t g, void* slab, void* slab_scales, int64_t ld_ss,
+    int32_t* masked_m, int32_t* d_status, moe_stream_t stream);
+
+/*
+ * moe_expand_from_slab -- [P3 实现拆解 item 3 masked_slab_to_expand: top-k
+ * weights fused on real rows only; ep_expand_init_m_indices_from_psum]. The
+ * inverse of moe_expand_to_slab: expanded row align(psum[e-1]) + j = slab row
+ * (e, j) for j < min(count_e, cap). With row_weights (bf16 payload only, indexed
+ * by expanded row) the stored row is bf16_RNE(fp32(w_r * v)). Scales are copied
+ * when both scale pointers are given. m_indices (optional) [R]: e on real rows,
+ * -1 on every other row. Expanded rows that are not real rows are not written.
+ * count_e > cap sets MOE_STATUS_OVERFLOW and rows past cap are not written.
+ * Launches: 1.
+ */
+moe_status_t moe_expand_from_slab(
+    const void* slab, int32_t elem_bytes, int32_t H, const void* slab_scales, int64_t ld_ss,
+    const int32_t* psum, int32_t L, int32_t align, int32_t cap, moe_scale_fmt_t fmt,
+    int32_t g, const float* row_weights, void* exp, int64_t R, void* exp_scales,
+    int64_t ld_es, int32_t* m_indices, int32_t* d_status, moe_stream_t stream);
+
+/* ------------------------------------------------------------------ */
+/* Per-token -> per-tensor requant                                      */
+/* ------------------------------------------------------------------ */
+
+/*
+ * fp8_requant_per_tensor -- [P2 实现拆解 items 1-2:
+ * fp8_per_token_to_per_tensor_quant; 风险与影响 item 3: plain fp32 per-token
+ * scales]. S = max_t s_tok[t] (S = 1 when T = 0 or every scale is 0);
+ * q_out[t, h] = RNE_e4m3( fp32( decode(q[t, h]) * fp32(s_tok[t] / S) ) ).
+ * Scales are finite and >= 0.
+ *   q [T, ldq] e4m3 (ldq % 16 == 0), s_tok [T] f32, q_out [T, H] e4m3 (H % 16 == 0),
+ *   d_scale_out [1] f32 receives S.
+ * Launches: 1.
+ */
+moe_status_t fp8_requant_per_tensor(
+    const void* q, int64_t ldq, const float* s_tok, int32_t T, int32_t H, void* q_out,
+    float* d_scale_out, moe_stream_t stream);
+
+/* ------------------------------------------------------------------ */
+/* Status                                                              */
+/* ------------------------------------------------------------------ */
+
+/* Waits for `stream`, reads the device status word and returns MOE_OK or the
+ * error its lowest set bit names (MOE_ERR_CUDA if the wait or copy fails). The
+ * non-graph "fail fast" check of [P3 风险与影响 item 1]. */
+moe_status_t moe_status_sync(const int32_t* d_status, moe_stream_t stream);
+
+/* Static description of a status code. */
+const char* moe_status_string(moe_status_t s);
+
+/* Version string of the library build. */
+const char* moe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOEPERM_H */

@@ -26,6 +26,8 @@ def dev():
     import torch
     if not torch.cuda.is_available():
         pytest.fail("gpu test selected but no CUDA device is visible")
+    from combine_fp8_quant_gb300 import build
+    build.build()
     import combine_fp8_quant_gb300 as mp
     mp.load()
     return mp

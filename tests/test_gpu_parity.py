@@ -1,0 +1,591 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle.
+
+Every output buffer is pre-filled with the same sentinel on both sides and
+compared bit for bit over its whole extent, so rows the definition does not
+name must stay untouched. Layout, payload and scale bytes must be identical;
+the combine must equal the oracle's fp32-FMA twin bit for bit and lie within
+one bf16 ulp of the fp64 sum (plus the fp32 accumulation floor K*2^-24*sum|w*y|).
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from gpu_util import DEV, bf16_dev, bf16_ulp, bits_equal, first_mismatch, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def assert_same(name, got, want):
+    assert bits_equal(got, want), f"{name}: first differing byte / count {first_mismatch(got, want)}"
+
+
+def compact_both(mp, ref, x, ids, w, H, K, E, L, b, g, fmt, n_live=None, ldx=None, with_rw=True):
+    T = ids.shape[0]
+    G = H // g
+    ldx = H if ldx is None else ldx
+    bound = ref.compact_bound(T * K, L, b)
+    r = {"xq": np.full((bound, H), 0xEE, np.uint8)}
+    r["sc"], ld = ref.scale_buffer(fmt, bound, G, fill=0xA5)
+    r["mi"] = np.full(bound, -7, np.int32)
+    r["s2d"] = np.full((T, K), -9, np.int32)
+    r["counts"] = np.full(L, -5, np.int32)
+    r["starts"] = np.full(L, -5, np.int32)
+    r["psum"] = np.full(L, -5, np.int32)
+    r["total"] = np.full(1, -3, np.int32)
+    r["rw"] = np.full(bound, np.nan, np.float32) if with_rw else None
+    d = {k: (to_dev(v.copy()) if v is not None else None) for k, v in r.items()}
+    nl = T if n_live is None else n_live
+    st_ref = ref.dispatch_compact(x, T, nl, H, ids, w, K, L, b, g, fmt, r["xq"], r["sc"], ld,
+                                  r["mi"], bound, r["s2d"], r["counts"], r["starts"], r["psum"],
+                                  r["total"], r["rw"], ldx=ldx)
+    ws = mp.Workspace(T, K, L, DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    nld = None if n_live is None else torch.tensor([n_live], dtype=torch.int32, device=DEV)
+    code = mp.moe_dispatch_compact(bf16_dev(x), ldx, T, nld, H, to_dev(ids), to_dev(w), K, E, L, b,
+                                   g, fmt, d["xq"], d["sc"], ld, d["mi"], bound, d["s2d"],
+                                   d["counts"], d["starts"], d["psum"], d["total"], d["rw"],
+                                   ws.buf, ws.nbytes, status)
+    assert code == mp.MOE_OK
+    torch.cuda.synchronize()
+    for k, v in r.items():
+        if v is not None:
+            assert_same(k, to_host(d[k], v), v)
+    assert int(status.item()) == st_ref
+    return r, d, ws
+
+
+def masked_both(mp, ref, x, ids, w, H, K, E, L, cap, g, fmt, n_live=None):
+    T = ids.shape[0]
+    G = H // g
+    r = {"xq": np.full((L * cap, H), 0xEE, np.uint8)}
+    r["sc"], ld = ref.scale_buffer(fmt, L * cap, G, fill=0xA5, blocks=L)
+    r["mm"] = np.full(L, -5, np.int32)
+    r["s2d"] = np.full((T, K), -9, np.int32)
+    r["rw"] = np.full(L * cap, np.nan, np.float32)
+    d = {k: to_dev(v.copy()) for k, v in r.items()}
+    nl = T if n_live is None else n_live
+    st_ref = ref.dispatch_masked(x, T, nl, H, ids, w, K, L, cap, g, fmt, r["xq"], r["sc"], ld,
+                                 r["mm"], r["s2d"], r["rw"])
+    ws = mp.Workspace(T, K, L, DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    nld = None if n_live is None else torch.tensor([n_live], dtype=torch.int32, device=DEV)
+    code = mp.moe_dispatch_masked(bf16_dev(x), H, T, nld, H, to_dev(ids), to_dev(w), K, E, L, cap,
+                                  g, fmt, d["xq"], d["sc"], ld, d["mm"], d["s2d"], d["rw"],
+                                  ws.buf, ws.nbytes, status)
+    assert code == mp.MOE_OK
+    torch.cuda.synchronize()
+    for k, v in r.items():
+        assert_same(k, to_host(d[k], v), v)
+    assert int(status.item()) == st_ref
+    return r, d, status
+
+
+def check_combine(mp, ref, y, s2d, w, H, n_live=None):
+    T, K = s2d.shape
+    R = y.shape[0]
+    want32 = ref.combine_f32(y, s2d, w, T, K, H)
+    want64, mass = ref.combine_f64(y, s2d, w, T, K, H)
+    out = torch.full((T, H), -12345.0, dtype=torch.bfloat16, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    nld = None if n_live is None else torch.tensor([n_live], dtype=torch.int32, device=DEV)
+    code = mp.moe_combine(bf16_dev(y), H, R, to_dev(s2d), None if w is None else to_dev(w), T, nld,
+                          K, H, out, status)
+    assert code == mp.MOE_OK
+    torch.cuda.synchronize()
+    got = to_host(out.view(torch.int16), want32)
+    n = T if n_live is None else n_live
+    assert_same("combine vs fp32-FMA twin", got[:n], want32[:n])
+    if n < T:
+        sentinel = to_host(torch.full((1,), -12345.0, dtype=torch.bfloat16).view(torch.int16), np.zeros(1, np.uint16))[0]
+        assert (got[n:] == sentinel).all(), "rows of non-live tokens untouched"
+    gf = synth.from_bf16_bits(got[:n]).astype(np.float64)
+    err = np.abs(gf - want64[:n])
+    tol = bf16_ulp(want64[:n]) + K * 2.0 ** -24 * mass[:n]
+    assert (err <= tol).all(), f"max err/tol {np.max(err / tol)}"
+    assert int(status.item()) == 0
+    return got
+
+
+# ---------------------------------------------------------------------------
+# quantisation
+# ---------------------------------------------------------------------------
+
+def test_e4m3_convert_exhaustive_via_quant_group(dev, ref):
+    """Every finite bf16 value x, scaled by 2^-e for several group exponents e:
+    each group of 32 holds one element 448*2^e that fixes the exponent and 31
+    test values with |x| <= 448*2^e. GPU bytes must equal the oracle's."""
+    H, g = 7168, 32
+    allb = np.arange(0, 0x10000, dtype=np.uint32).astype(np.uint16)
+    vals = synth.from_bf16_bits(allb)
+    finite = np.isfinite(vals)
+    for e in (-42, -20, -6, 0, 3, 9, 60, 119):
+        amax = np.float32(448.0 * 2.0 ** e)
+        amax_b = synth.to_bf16_bits(np.array([amax], np.float32))[0]
+        test = allb[finite & (np.abs(vals) <= amax)]
+        ngroups = -(-test.size // 31)
+        pad = np.resize(test, ngroups * 31) if test.size else np.zeros(31, np.uint16)
+        groups = np.concatenate([np.full((ngroups, 1), amax_b, np.uint16), pad.reshape(ngroups, 31)], axis=1)
+        per_row = H // g
+        nrows = -(-ngroups // per_row)
+        rows = np.zeros((nrows * per_row, g), np.uint16)
+        rows[:] = amax_b
+        rows[:ngroups] = groups
+        x = rows.reshape(nrows, H)
+        rxq = np.full((nrows, H), 0xEE, np.uint8)
+        rsc, ld = ref.scale_buffer("u8", nrows, H // g)
+        ref.quant_group(x, nrows, nrows, H, g, "u8", rxq, rsc, ld)
+        assert (rsc == 127 + e).all()
+        out = dev.quant_group(bf16_dev(x), group_size=g, scale_fmt="u8")
+        torch.cuda.synchronize()
+        assert_same(f"xq e={e}", to_host(out["xq"], rxq), rxq)
+        assert_same(f"scales e={e}", to_host(out["scales"], rsc), rsc)
+
+
+@pytest.mark.parametrize("fmt,g,T,H", [("packed", 128, 50, 640), ("u8", 128, 33, 7168),
+                                       ("f32", 128, 17, 1152), ("u8", 32, 5, 224),
+                                       ("packed", 128, 257, 7168)])
+def test_quant_group_formats(dev, ref, fmt, g, T, H):
+    rng = np.random.default_rng(T + H)
+    x = synth.normal_bf16(rng, (T, H), outlier_frac=0.02)
+    x[0, :g] = 0                     # an all-zero group
+    G = H // g
+    rxq = np.full((T, H), 0xEE, np.uint8)
+    rsc, ld = ref.scale_buffer(fmt, T, G, fill=0x5A)
+    ref.quant_group(x, T, T, H, g, fmt, rxq, rsc, ld)
+    dxq, dsc = to_dev(rxq.copy()), to_dev(rsc.copy())
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    assert dev.moe_quant_group(bf16_dev(x), H, T, None, H, g, fmt, dxq, dsc, ld, st) == 0
+    torch.cuda.synchronize()
+    assert_same("xq", to_host(dxq, rxq), rxq)
+    assert_same("scales", to_host(dsc, rsc), rsc)
+
+
+def test_mxfp8_sparse_live_rows_full_size(dev, ref):
+    """24576-row receive buffer, 112 live rows, the rest NaN/Inf garbage: only
+    live rows are read and written; group-32 e8m0, 224 scales per row."""
+    d = synth.mxfp8(0)
+    c = d["cfg"]
+    T_cap, n, H, g = c["T_cap"], c["n_live"], c["H"], c["g"]
+    assert H // g == 224
+    rxq = np.full((T_cap, H), 0xEE, np.uint8)
+    rsc, ld = ref.scale_buffer("u8", T_cap, H // g)
+    assert ref.quant_group(d["x"], T_cap, n, H, g, "u8", rxq, rsc, ld) == 0
+    dxq, dsc = to_dev(rxq), to_dev(rsc)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    nl = torch.tensor([n], dtype=torch.int32, device=DEV)
+    assert dev.moe_quant_group(bf16_dev(d["x"]), H, T_cap, nl, H, g, "u8", dxq, dsc, ld, st) == 0
+    torch.cuda.synchronize()
+    assert_same("xq", to_host(dxq, rxq), rxq)
+    assert_same("scales", to_host(dsc, rsc), rsc)
+    assert int(st.item()) == 0
+    # empty live batch: nothing written
+    nl.zero_()
+    before = dxq.clone()
+    assert dev.moe_quant_group(bf16_dev(d["x"]), H, T_cap, nl, H, g, "u8", dxq, dsc, ld, st) == 0
+    torch.cuda.synchronize()
+    assert torch.equal(before, dxq)
+    # empty tensor API: scale shape (0, 224)
+    out = dev.quant_group(torch.empty((0, H), dtype=torch.bfloat16, device=DEV), group_size=32, scale_fmt="u8")
+    assert tuple(out["scales"].shape) == (0, 224) and out["scales"].dtype == torch.uint8
+    # live count above the buffer: clamped to the buffer, flagged
+    x2 = synth.normal_bf16(np.random.default_rng(1), (64, H))
+    st.zero_()
+    small_q = torch.empty((64, H), dtype=torch.uint8, device=DEV)
+    small_s = torch.empty((64, H // g), dtype=torch.uint8, device=DEV)
+    nl.fill_(65)
+    assert dev.moe_quant_group(bf16_dev(x2), H, 64, nl, H, g, "u8", small_q, small_s, H // g, st) == 0
+    assert dev.moe_status_sync(st) == dev.MOE_ERR_LIVE_OVERFLOW
+
+
+# ---------------------------------------------------------------------------
+# compact dispatch
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("seed", range(5))
+@pytest.mark.parametrize("fmt", ["packed", "u8", "f32"])
+def test_dispatch_compact_tiny(dev, ref, seed, fmt):
+    d = synth.tiny(seed)
+    c = d["cfg"]
+    compact_both(dev, ref, d["x"], d["topk_ids"], d["topk_weights"], c["H"], c["K"], c["E"], c["L"],
+                 c["block_e"], c["g"], fmt)
+
+
+@pytest.mark.parametrize("fmt", ["packed", "u8", "f32"])
+def test_dispatch_compact_tiles_and_ragged_tail(dev, ref, fmt):
+    d = synth.prefill(1, T=333, H=1536)
+    compact_both(dev, ref, d["x"], d["topk_ids"], d["topk_weights"], 1536, 8, 256, 256, 128, 128, fmt)
+
+
+def test_dispatch_compact_nondividing_groups_and_dropped(dev, ref):
+    """H = 640 (5 groups: the last packed word is half padding), 40 experts of
+    which 20 are local, block_e = 16."""
+    rng = np.random.default_rng(3)
+    T, K, H = 97, 4, 640
+    x = synth.normal_bf16(rng, (T, H))
+    ids = synth.uniform_topk(rng, T, 40, K)
+    ids[5, 0] = -1
+    w = synth.softmax_weights(rng, T, K)
+    for fmt in ("packed", "u8"):
+        compact_both(dev, ref, x, ids, w, H, K, 40, 20, 16, 128, fmt)
+
+
+def test_dispatch_compact_live_tokens_and_stride(dev, ref):
+    rng = np.random.default_rng(4)
+    T, K, H, ldx = 200, 8, 1024, 1088
+    xf = synth.normal_bf16(rng, (T, ldx))
+    xf[150:] = synth.garbage_bf16_rows(T - 150, ldx)
+    ids = synth.uniform_topk(rng, T, 64, K)
+    ids[150:] = 0x7FFFFFF0          # never read
+    w = synth.softmax_weights(rng, T, K)
+    r, d, _ = compact_both(dev, ref, xf, ids, w, H, K, 64, 64, 128, 128, "packed", n_live=150, ldx=ldx)
+    assert (r["s2d"][150:] == -1).all()
+
+
+@pytest.mark.parametrize("T,K,L,H", [(4096, 8, 256, 128), (40000, 8, 300, 128), (1, 1, 1, 128),
+                                     (3, 2, 1024, 128), (1000, 16, 7, 256)])
+def test_dispatch_compact_chunking(dev, ref, T, K, L, H):
+    """Route-plan chunk sizes S = 1, 4, 16 and 64 (up to 20 chunks), one CTA, L = 1024."""
+    rng = np.random.default_rng(T + L)
+    x = synth.normal_bf16(rng, (T, H))
+    E = max(L, 2 * K)
+    ids = synth.zipf_topk(rng, T, E, K, n_empty=min(12, E - K)) if T > 1 else synth.uniform_topk(rng, T, E, K)
+    w = synth.softmax_weights(rng, T, K)
+    compact_both(dev, ref, x, ids, w, H, K, E, L, 128, 128, "packed")
+
+
+def test_dispatch_compact_degenerate(dev, ref):
+    rng = np.random.default_rng(6)
+    H = 256
+    x = synth.normal_bf16(rng, (64, H))
+    w = np.ones((64, 4), np.float32)
+    compact_both(dev, ref, x, np.full((64, 4), -1, np.int32), w, H, 4, 8, 8, 128, 128, "packed")  # all dropped
+    compact_both(dev, ref, x, np.full((64, 4), 3, np.int32), w, H, 4, 8, 8, 128, 128, "u8")      # one hot expert
+    compact_both(dev, ref, x[:0], np.zeros((0, 4), np.int32), w[:0], H, 4, 8, 8, 128, 128, "packed")  # T = 0
+
+
+def test_dispatch_compact_mxfp8_group32(dev, ref):
+    d = synth.mxfp8(2, T_cap=112, n_live=112)
+    compact_both(dev, ref, d["x"], d["topk_ids"], d["topk_weights"], 7168, 8, 256, 256, 128, 32, "u8")
+
+
+# ---------------------------------------------------------------------------
+# masked dispatch
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("seed", range(3))
+@pytest.mark.parametrize("fmt", ["packed", "u8"])
+def test_dispatch_masked_decode(dev, ref, seed, fmt):
+    d = synth.decode(seed)
+    c = d["cfg"]
+    assert ref.should_use_masked(c["E"], c["L"])
+    masked_both(dev, ref, d["x"], d["topk_ids"], d["topk_weights"], c["H"], c["K"], c["E"], c["L"],
+                c["cap"], c["g"], fmt)
+
+
+def test_dispatch_masked_overflow_fails_fast(dev, ref):
+    rng = np.random.default_rng(8)
+    T, K, H = 64, 8, 512
+    x = synth.normal_bf16(rng, (T, H))
+    ids = synth.uniform_topk(rng, T, 8, K)       # ~64 slots per local expert
+    w = synth.softmax_weights(rng, T, K)
+    r, d, status = masked_both(dev, ref, x, ids, w, H, K, 8, 4, 40, 128, "packed")
+    assert dev.moe_status_sync(status) == dev.MOE_ERR_OVERFLOW
+    masked_both(dev, ref, x, ids, w, H, K, 8, 4, 64, 128, "f32")   # exactly at capacity
+
+
+def test_dispatch_masked_live_tokens(dev, ref):
+    rng = np.random.default_rng(9)
+    T, K, H = 96, 8, 1024
+    x = synth.normal_bf16(rng, (T, H))
+    x[70:] = synth.garbage_bf16_rows(T - 70, H)
+    ids = synth.uniform_topk(rng, T, 128, K)
+    w = synth.softmax_weights(rng, T, K)
+    masked_both(dev, ref, x, ids, w, H, K, 128, 16, 64, 128, "packed", n_live=70)
+
+
+# ---------------------------------------------------------------------------
+# combine
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("K", [1, 3, 8, 13])
+def test_combine_random_rows(dev, ref, K):
+    rng = np.random.default_rng(K)
+    T, H, R = 77, 1536, 500
+    y = synth.normal_bf16(rng, (R, H))
+    s2d = rng.integers(-1, R, size=(T, K)).astype(np.int32)
+    s2d[3] = -1
+    w = synth.softmax_weights(rng, T, K)
+    check_combine(dev, ref, y, s2d, w, H)
+    check_combine(dev, ref, y, s2d, None, H)
+
+
+def test_combine_live_tokens_and_bad_index(dev, ref):
+    rng = np.random.default_rng(12)
+    T, K, H, R = 40, 8, 512, 100
+    y = synth.normal_bf16(rng, (R, H))
+    s2d = rng.integers(-1, R, size=(T, K)).astype(np.int32)
+    w = synth.softmax_weights(rng, T, K)
+    check_combine(dev, ref, y, s2d, w, H, n_live=25)
+    bad = s2d.copy()
+    bad[2, 1] = R + 7
+    out = torch.zeros((T, H), dtype=torch.bfloat16, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    assert dev.moe_combine(bf16_dev(y), H, R, to_dev(bad), to_dev(w), T, None, K, H, out, st) == 0
+    assert dev.moe_status_sync(st) == dev.MOE_ERR_BAD_LAYOUT
+    fixed = bad.copy()
+    fixed[2, 1] = -1
+    want = ref.combine_f32(y, fixed, w, T, K, H)
+    assert_same("combine skipping the bad slot", to_host(out.view(torch.int16), want), want)
+
+
+def test_dispatch_then_combine_masked_equals_compact(dev, ref):
+    """PR #33128 test idea on the GPU: expert outputs that depend only on
+    (expert, token) give bit-identical combines in both layouts."""
+    d = synth.decode(1, T=128)
+    c = d["cfg"]
+    T, K, E, L, cap, H = 128, 8, 256, 32, 128, 1024
+    x = d["x"][:, :H].copy()
+    ids, w = d["topk_ids"], d["topk_weights"]
+    rc, dc, _ = compact_both(dev, ref, x, ids, w, H, K, E, L, 128, 128, "packed")
+    rm, dm, _ = masked_both(dev, ref, x, ids, w, H, K, E, L, cap, 128, "packed")
+    rng = np.random.default_rng(5)
+    table = synth.normal_bf16(rng, (L, T, H))
+    yc = np.zeros((rc["xq"].shape[0], H), np.uint16)
+    ym = np.zeros((L * cap, H), np.uint16)
+    flat = ids.reshape(-1)
+    for a in range(T * K):
+        e = flat[a]
+        if 0 <= e < L:
+            yc[rc["s2d"].reshape(-1)[a]] = table[e, a // K]
+            ym[rm["s2d"].reshape(-1)[a]] = table[e, a // K]
+    oc = check_combine(dev, ref, yc, rc["s2d"], w, H)
+    om = check_combine(dev, ref, ym, rm["s2d"], w, H)
+    assert np.array_equal(oc, om)
+
+
+# ---------------------------------------------------------------------------
+# repack
+# ---------------------------------------------------------------------------
+
+def build_layout(counts, align):
+    starts, psum, prev = [], [], 0
+    for cnt in counts:
+        st = -(-prev // align) * align
+        starts.append(st)
+        psum.append(st + cnt)
+        prev = st + cnt
+    return np.array(psum, np.int32), starts, max(-(-prev // align) * align, 1)
+
+
+def repack_both(dev, ref, exp, eb, H, psum, L, align, cap, fmt=None, g=128, exp_sc=None, ld_es=0,
+                weights=None):
+    R = exp.shape[0]
+    G = H // g
+    slab = np.full((L * cap, H * eb), 0xEE, np.uint8)
+    mm = np.full(L, -1, np.int32)
+    if exp_sc is not None:
+        ssc, ld_ss = ref.scale_buffer(fmt, L * cap, G, fill=0x3C, blocks=L)
+    else:
+        ssc, ld_ss = None, 0
+    st_ref = ref.expand_to_slab(exp, eb, H, R, exp_sc, ld_es, psum, L, align, cap, fmt or "u8", g,
+                                slab, ssc, ld_ss, mm)
+    d_slab, d_mm = to_dev(np.full_like(slab, 0xEE)), to_dev(np.full_like(mm, -1))
+    d_ssc = to_dev(ref.scale_buffer(fmt, L * cap, G, fill=0x3C, blocks=L)[0]) if exp_sc is not None else None
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    assert dev.moe_expand_to_slab(to_dev(exp), eb, H, R, to_dev(exp_sc) if exp_sc is not None else None,
+                                  ld_es, to_dev(psum), L, align, cap, fmt or "u8", g, d_slab, d_ssc,
+                                  ld_ss, d_mm, st) == 0
+    torch.cuda.synchronize()
+    assert_same("slab", to_host(d_slab, slab), slab)
+    assert_same("masked_m", to_host(d_mm, mm), mm)
+    if ssc is not None:
+        assert_same("slab scales", to_host(d_ssc, ssc), ssc)
+    assert int(st.item()) == st_ref
+    # back to the expanded layout
+    back = np.full_like(exp, 0xDD)
+    mi = np.full(R, 77, np.int32)
+    bsc = ref.scale_buffer(fmt, R, G, fill=0x11)[0] if exp_sc is not None else None
+    st2_ref = ref.expand_from_slab(slab, eb, H, ssc, ld_ss, psum, L, align, cap, fmt or "u8", g,
+                                   weights, back, R, bsc, ld_es, mi)
+    d_back, d_mi = to_dev(np.full_like(exp, 0xDD)), to_dev(np.full(R, 77, np.int32))
+    d_bsc = to_dev(ref.scale_buffer(fmt, R, G, fill=0x11)[0]) if exp_sc is not None else None
+    st.zero_()
+    assert dev.moe_expand_from_slab(d_slab, eb, H, d_ssc, ld_ss, to_dev(psum), L, align, cap,
+                                    fmt or "u8", g, to_dev(weights) if weights is not None else None,
+                                    d_back, R, d_bsc, ld_es, d_mi, st) == 0
+    torch.cuda.synchronize()
+    assert_same("expanded", to_host(d_back, back), back)
+    assert_same("m_indices", to_host(d_mi, mi), mi)
+    if bsc is not None:
+        assert_same("expanded scales", to_host(d_bsc, bsc), bsc)
+    assert int(st.item()) == st2_ref
+    return st_ref, slab, back
+
+
+@pytest.mark.parametrize("counts", [[3, 0, 5, 1], [0, 0, 0, 0], [0, 17, 0, 0], [8, 8, 8, 8], [1, 0, 0, 9]])
+@pytest.mark.parametrize("eb", [1, 2])
+def test_repack_build_layout_cases(dev, ref, counts, eb):
+    """The digest's _build_layout cases: empty experts, one hot expert, counts
+    at / over capacity; distinct per-row values with alternating column gain."""
+    H, align, cap, L = 64, 4, 8, len(counts)
+    psum, starts, R = build_layout(counts, align)
+    base = np.zeros((R, H), np.float32)
+    gain = 1.0 + (np.arange(H) % 2)
+    for s0, cnt in zip(starts, counts):
+        for j in range(cnt):
+            base[s0 + j] = float((s0 + j) % 200 + 1) * gain
+    if eb == 2:
+        exp = synth.to_bf16_bits(base).view(np.uint8).reshape(R, 2 * H)
+    else:
+        exp = synth.to_e4m3_bits(np.minimum(base, 448)).reshape(R, H)
+    st, _, _ = repack_both(dev, ref, exp, eb, H, psum, L, align, cap)
+    assert bool(st & ref.ST_OVERFLOW) == any(cnt > cap for cnt in counts)
+
+
+@pytest.mark.parametrize("fmt", ["packed", "u8", "f32"])
+def test_repack_config_fp8_with_quantizer_scales(dev, ref, fmt):
+    """Requant/repack config: 64 experts, 128-aligned psum over 4096 expanded
+    rows, e4m3 payload and scales made by each side's own quantiser."""
+    d = synth.requant(0)
+    c = d["cfg"]
+    rng = d["rng"]
+    L, align, H, g = c["L"], c["align"], c["H"], 128
+    counts = synth.repack_counts(rng, L, c["blocks"], align)
+    psum, starts, R = build_layout(counts, align)
+    assert R == c["T"]
+    cap = int(-(-counts.max() // 128) * 128)
+    x = synth.normal_bf16(rng, (R, H))
+    G = H // g
+    exp = np.zeros((R, H), np.uint8)
+    esc, ld_es = ref.scale_buffer(fmt, R, G, fill=0)
+    ref.quant_group(x, R, R, H, g, fmt, exp, esc, ld_es)
+    # the GPU quantiser must produce the same bytes
+    gq = dev.quant_group(bf16_dev(x), group_size=g, scale_fmt=fmt)
+    torch.cuda.synchronize()
+    assert_same("gpu quantiser payload", to_host(gq["xq"], exp), exp)
+    assert_same("gpu quantiser scales", to_host(gq["scales"], esc), esc)
+    st, _, _ = repack_both(dev, ref, exp, 1, H, psum, L, align, cap, fmt=fmt, g=g, exp_sc=esc, ld_es=ld_es)
+    assert st == 0
+    assert cap > 128, "the seeded counts give an expert with more than one block"
+    # overflow: capacity one block below the largest expert
+    st, _, _ = repack_both(dev, ref, exp, 1, H, psum, L, align, cap - 128, fmt=fmt, g=g, exp_sc=esc, ld_es=ld_es)
+    assert st & ref.ST_OVERFLOW
+
+
+def test_repack_weighted_bf16(dev, ref):
+    rng = np.random.default_rng(21)
+    counts = [5, 0, 130, 1, 77]
+    H, align, cap, L = 512, 128, 256, 5
+    psum, starts, R = build_layout(counts, align)
+    exp = synth.normal_bf16(rng, (R, H)).view(np.uint8).reshape(R, 2 * H)
+    wts = rng.random(R).astype(np.float32)
+    repack_both(dev, ref, exp, 2, H, psum, L, align, cap, weights=wts)
+
+
+def test_repack_bad_layout_flagged(dev, ref):
+    H, L, align, cap = 16, 3, 4, 8
+    exp = np.zeros((12, H), np.uint8)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    slab = torch.zeros((L * cap, H), dtype=torch.uint8, device=DEV)
+    mm = torch.zeros(L, dtype=torch.int32, device=DEV)
+    for psum in ([3, 2, 9], [3, 6, 20]):
+        st.zero_()
+        assert dev.moe_expand_to_slab(to_dev(exp), 1, H, 12, None, 0, to_dev(np.array(psum, np.int32)),
+                                      L, align, cap, "u8", 128, slab, None, 0, mm, st) == 0
+        assert dev.moe_status_sync(st) == dev.MOE_ERR_BAD_LAYOUT
+
+
+# ---------------------------------------------------------------------------
+# requant
+# ---------------------------------------------------------------------------
+
+def requant_both(dev, ref, q, s):
+    T, H = q.shape
+    want, S = ref.requant(q, s, T, H)
+    out = torch.full((T, H), 0xEE, dtype=torch.uint8, device=DEV)
+    dS = torch.zeros(1, dtype=torch.float32, device=DEV)
+    assert dev.fp8_requant_per_tensor(to_dev(q), H, to_dev(s), T, H, out, dS) == 0
+    torch.cuda.synchronize()
+    assert_same("requant payload", to_host(out, want), want)
+    assert float(dS.item()) == S
+
+
+def test_requant_config_full(dev, ref):
+    d = synth.requant(0)
+    requant_both(dev, ref, d["q"], d["s_tok"])
+
+
+@pytest.mark.parametrize("T,H", [(1, 16), (37, 1040), (300, 7168)])
+def test_requant_shapes(dev, ref, T, H):
+    d = synth.requant(T, T=T, H=H)
+    requant_both(dev, ref, d["q"], d["s_tok"])
+
+
+def test_requant_edge_cases(dev, ref):
+    q = np.array([[0x38, 0xC0, 0x00, 0x7E] * 4, [0x38, 0x44, 0x80, 0x7E] * 4], np.uint8)
+    requant_both(dev, ref, q, np.array([2.0, 1.0], np.float32))
+    requant_both(dev, ref, q, np.zeros(2, np.float32))
+    dS = torch.zeros(1, dtype=torch.float32, device=DEV)
+    assert dev.fp8_requant_per_tensor(None, 16, None, 0, 16, None, dS) == 0
+    torch.cuda.synchronize()
+    assert float(dS.item()) == 1.0
+
+
+# ---------------------------------------------------------------------------
+# CUDA graph capture and replay
+# ---------------------------------------------------------------------------
+
+def test_graph_capture_replay_new_routing(dev, ref):
+    T, H, K, E, L, b, g = 256, 1024, 8, 64, 64, 128, 128
+    d0 = synth.prefill(0, T=T, H=H)
+    ids0 = np.ascontiguousarray(d0["topk_ids"] % E).astype(np.int32)
+    x = bf16_dev(d0["x"])
+    ids = to_dev(ids0)
+    w = to_dev(d0["topk_weights"])
+    bound = dev.moe_compact_bound(T * K, L, b)
+    rng = np.random.default_rng(3)
+    y = bf16_dev(synth.normal_bf16(rng, (bound, H)))
+    ws = dev.Workspace(T, K, L, DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        out = dev.dispatch_compact(x, ids, w, E, L, block_e=b, group_size=g, scale_fmt="packed",
+                                   workspace=ws, status=st)
+        comb = dev.combine(y, out["src2dst"], w, status=st)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        out = dev.dispatch_compact(x, ids, w, E, L, block_e=b, group_size=g, scale_fmt="packed",
+                                   workspace=ws, status=st)
+        comb = dev.combine(y, out["src2dst"], w, status=st, out=comb)
+    for seed in (1, 2):
+        dn = synth.prefill(seed, T=T, H=H)
+        idn = np.ascontiguousarray(dn["topk_ids"] % E).astype(np.int32)
+        x.copy_(bf16_dev(dn["x"]))
+        ids.copy_(to_dev(idn))
+        w.copy_(to_dev(dn["topk_weights"]))
+        graph.replay()
+        torch.cuda.synchronize()
+        rxq = np.zeros((bound, H), np.uint8)
+        rsc, ld = ref.scale_buffer("packed", bound, H // g)
+        rmi = np.zeros(bound, np.int32)
+        rs2d = np.zeros((T, K), np.int32)
+        rc, rs, rp = (np.zeros(L, np.int32) for _ in range(3))
+        rt = np.zeros(1, np.int32)
+        ref.dispatch_compact(dn["x"], T, T, H, idn, dn["topk_weights"], K, L, b, g, "packed", rxq,
+                             rsc, ld, rmi, bound, rs2d, rc, rs, rp, rt)
+        assert np.array_equal(out["src2dst"].cpu().numpy(), rs2d)
+        assert np.array_equal(out["m_indices"].cpu().numpy(), rmi)
+        rows = rs2d[rs2d >= 0]
+        assert np.array_equal(out["xq"].cpu().numpy()[rows], rxq[rows])
+        ynp = to_host(y.view(torch.int16), np.zeros((bound, H), np.uint16))
+        want = ref.combine_f32(ynp, rs2d, dn["topk_weights"], T, K, H)
+        assert_same("graph combine", to_host(comb.view(torch.int16), want), want)
+    assert int(st.item()) == 0
