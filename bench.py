@@ -112,9 +112,18 @@ class Clocks:
 # CPU oracle baseline (bounded sample of the same workload)
 # ---------------------------------------------------------------------------
 
+_PREFILL_CACHE = {}
+
+
+def prefill_inputs(seed=0):
+    if seed not in _PREFILL_CACHE:
+        _PREFILL_CACHE[seed] = synth.prefill(seed)
+    return _PREFILL_CACHE[seed]
+
+
 def oracle_sample(tokens: int, reps: int):
     import oracle as ref
-    d = synth.prefill(0)
+    d = prefill_inputs(0)
     c = d["cfg"]
     T, H, K, L, b, g = tokens, c["H"], c["K"], c["L"], c["block_e"], c["g"]
     x, ids, w = d["x"][:T].copy(), d["topk_ids"][:T].copy(), d["topk_weights"][:T].copy()
@@ -191,7 +200,7 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device(f"cuda:{local_rank}")
     torch.cuda.set_device(dev)
 
-    d = synth.prefill(rank)
+    d = synth.prefill(rank, T=args.tokens)
     c = d["cfg"]
     T, H, K, E, L, b, g = c["T"], c["H"], c["K"], c["E"], c["L"], c["block_e"], c["g"]
     x_h = torch.from_numpy(d["x"].view(np.int16)).view(torch.bfloat16)
@@ -256,11 +265,18 @@ def run_ours(args, rank, world, local_rank):
     ms_step = sum(t_step) / K_steps
     ms_disp = sum(t_disp) / K_steps
     ms_comb = sum(t_comb) / K_steps
-    if world > 1:
-        tt = torch.tensor([ms_step, ms_disp, ms_comb], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_step, ms_disp, ms_comb = tt.tolist()
+    ms_step, ms_disp, ms_comb = max_over_ranks([ms_step, ms_disp, ms_comb], world, dev)
     assert mp.moe_status_sync(st) == 0
+
+    if args.only_step:
+        if rank == 0:
+            hbm, _ = peaks()
+            print(json.dumps({"only_step": True, "T": T, "ms_per_step": ms_step,
+                              "dispatch_us": ms_disp * 1e3, "combine_us": ms_comb * 1e3,
+                              "dispatch_gbs": db / (ms_disp * 1e-3) / 1e9,
+                              "combine_gbs": cb / (ms_comb * 1e-3) / 1e9, "hbm_peak": hbm,
+                              "clocks": clk}), flush=True)
+        return
 
     # -- end to end through the C ABI with host buffers -------------------------
     x_p, ids_p, w_p = x_h.pin_memory(), ids_h.pin_memory(), w_h.pin_memory()
@@ -290,10 +306,7 @@ def run_ours(args, rank, world, local_rank):
     e1.record()
     torch.cuda.synchronize()
     ms_e2e = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        tt = torch.tensor([ms_e2e], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_e2e = tt.item()
+    ms_e2e = max_over_ranks([ms_e2e], world, dev)[0]
 
     # -- other hot-path rows on their own workloads --------------------------------
     rows = other_rows(mp, dev, flush) if rank == 0 else None
@@ -302,7 +315,7 @@ def run_ours(args, rank, world, local_rank):
         return
     hbm, peak_kind = peaks()
     step_bytes = (db + cb) * world
-    value = step_bytes / (ms_step * 1e-3) / 1e9
+    value = whole_job_gbs(db + cb, world, ms_step)
     comb_gbs = cb / (ms_comb * 1e-3) / 1e9
     disp_gbs = db / (ms_disp * 1e-3) / 1e9
     traffic = load_traffic("combine")
@@ -333,7 +346,7 @@ def run_ours(args, rank, world, local_rank):
                               "achieved": disp_gbs, "peak": hbm, "unit": "GB/s",
                               "frac": disp_gbs / hbm, "traffic": load_traffic("dispatch")},
         "cpu_baseline": {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")},
-        "e2e": {"value": step_bytes / (ms_e2e * 1e-3) / 1e9, "unit": UNIT,
+        "e2e": {"value": whole_job_gbs(db + cb, world, ms_e2e), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e,
                 "api": "moe_dispatch_compact + moe_combine (C ABI), pinned host buffers"},
         "gpu_launches": 3 * K_steps,
@@ -343,15 +356,44 @@ def run_ours(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+def max_over_ranks(values, world, device=None):
+    """Element-wise max of per-rank timings (a barrier-free all-reduce); the
+    whole job is as slow as its slowest replica."""
+    if world <= 1:
+        return list(values)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_gbs(bytes_per_rank, world, ms):
+    """Aggregate throughput: all ranks' algorithmic bytes over the max time."""
+    return bytes_per_rank * world / (ms * 1e-3) / 1e9
+
+
+def kernel_source_sha(files):
+    import hashlib
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "combine_fp8_quant_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def load_traffic(which):
-    """DRAM bytes per launch from the committed ncu summary, if one matches the
-    current kernels (null otherwise)."""
+    """DRAM bytes (read + write) per launch of a kernel, from the committed ncu
+    summary profiles/traffic.json -- null when absent or when the kernel's
+    source has changed since the counters were taken."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
-        d = json.load(f)
-    return d.get(which)
+        d = json.load(f).get(which)
+    if not d or d.get("source_sha") != kernel_source_sha(d.get("sources", [])):
+        return None
+    return d.get("bytes_per_launch")
 
 
 def time_call(fn, flush, reps=20):
@@ -481,6 +523,11 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--only-step", action="store_true",
+                    help="time the dispatch + combine step only (no e2e, other rows or CPU "
+                         "baseline); used for profiler captures")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="override T of the prefill workload (profiling smaller cases)")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -68,7 +68,6 @@ moe_status_t check_common(const DispatchCommon& c) {
     if (!c.x || !aligned16(c.x) || c.ldx < c.H || c.ldx % 8) return MOE_ERR_INVALID_ARG;
     if (!c.ids || !c.src2dst) return MOE_ERR_INVALID_ARG;
   }
-  if (!c.xq || !aligned16(c.xq) || !c.scales || !aligned16(c.scales)) return MOE_ERR_INVALID_ARG;
   if (c.row_weights && !c.w) return MOE_ERR_INVALID_ARG;
   if (!c.ws || !aligned16(c.ws) || c.ws_bytes < moe_workspace_bytes(c.T, c.K, c.L))
     return MOE_ERR_INVALID_ARG;
@@ -150,8 +149,10 @@ moe_status_t moe_dispatch_compact(
   if (block_e < 1) return MOE_ERR_INVALID_ARG;
   const int64_t need = moe_compact_bound((int64_t)T * K, L, block_e);
   if (bound < need || bound >= (int64_t(1) << 31)) return MOE_ERR_INVALID_ARG;
-  if (!m_indices || !counts || !starts || !psum || !total) return MOE_ERR_INVALID_ARG;
-  if (!ld_ok(fmt, ld_s, bound, H / g)) return MOE_ERR_INVALID_ARG;
+  if (!counts || !starts || !psum || !total) return MOE_ERR_INVALID_ARG;
+  if (bound > 0 && (!m_indices || !xq || !aligned16(xq) || !scales || !aligned16(scales)))
+    return MOE_ERR_INVALID_ARG;
+  if (bound > 0 && !ld_ok(fmt, ld_s, bound, H / g)) return MOE_ERR_INVALID_ARG;
   return run_dispatch(c, kModeCompact, block_e, 0, m_indices, bound, counts, starts, psum,
                       total, nullptr, d_status, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -168,7 +169,7 @@ moe_status_t moe_dispatch_masked(
   moe_status_t st = check_common(c);
   if (st != MOE_OK) return st;
   if (cap < 1 || (int64_t)L * cap >= (int64_t(1) << 31)) return MOE_ERR_INVALID_ARG;
-  if (!masked_m) return MOE_ERR_INVALID_ARG;
+  if (!masked_m || !xq || !aligned16(xq) || !scales || !aligned16(scales)) return MOE_ERR_INVALID_ARG;
   if (!ld_ok(fmt, ld_s, cap, H / g)) return MOE_ERR_INVALID_ARG;
   return run_dispatch(c, kModeMasked, 1, cap, nullptr, 0, nullptr, nullptr, nullptr, nullptr,
                       masked_m, d_status, reinterpret_cast<cudaStream_t>(stream));
@@ -286,9 +287,9 @@ moe_status_t moe_status_sync(const int32_t* d_status, moe_stream_t stream) {
   if (cudaMemcpyAsync(&v, d_status, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
-  if (v & MOE_STATUS_OVERFLOW) return MOE_ERR_OVERFLOW;
-  if (v & MOE_STATUS_LIVE_OVERFLOW) return MOE_ERR_LIVE_OVERFLOW;
   if (v & MOE_STATUS_BAD_LAYOUT) return MOE_ERR_BAD_LAYOUT;
+  if (v & MOE_STATUS_LIVE_OVERFLOW) return MOE_ERR_LIVE_OVERFLOW;
+  if (v & MOE_STATUS_OVERFLOW) return MOE_ERR_OVERFLOW;
   return MOE_OK;
 }
 

@@ -4,12 +4,15 @@
 //   out[t, :] = bf16_RNE( sum_{k : src2dst[t,k] >= 0} w[t,k] * y[src2dst[t,k], :] )
 //   fp32 accumulator from +0, one fused multiply-add per slot in ascending k.
 //
-// Design: persistent grid; a CTA owns one token at a time. Threads < K load the
-// token's rows and weights into shared memory (double-buffered, one barrier
-// per token); each thread then owns 8-element chunks and issues the loads of
-// up to 8 source rows before the first FMA, so a thread keeps 8 (two chunks:
-// 16) independent 16-byte loads in flight. y is read once per kept slot and
-// out written once: the kernel is bound by HBM reads.
+// Design: persistent grid; a CTA owns one token at a time and each thread owns
+// 8-element (16-byte) chunks of it. There is no barrier: every thread reads
+// the token's K row indices and weights itself (the warp's loads of the same
+// words are one broadcast transaction), and the indices of the CTA's NEXT
+// token are prefetched into registers while the current token is processed,
+// so their latency never sits in front of the row loads. A thread issues the
+// loads of up to 8 source rows for each of its CPT chunks before the first
+// FMA. y is read once per kept slot and out written once: the kernel is bound
+// by HBM reads.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -17,32 +20,44 @@ namespace moeperm {
 
 namespace {
 
-constexpr int kMaxK = 32;
 constexpr int kBatch = 8;   // source rows loaded before accumulating
 constexpr int kCPT = 2;     // 8-element chunks per thread per pass
 
-__global__ void __launch_bounds__(512) combine_kernel(CombineArgs p) {
-  __shared__ int s_row[2][kMaxK];
-  __shared__ float s_w[2][kMaxK];
-  const int tid = threadIdx.x, bd = blockDim.x;
-  const int nch = p.H / 8;
-  const int n_live = live_count(p.d_num_tokens, p.T, p.status, blockIdx.x == 0 && tid == 0);
-  int it = 0;
-  for (int t = blockIdx.x; t < n_live; t += gridDim.x, ++it) {
-    const int buf = it & 1;
-    if (tid < p.K) {
-      const int64_t a = (int64_t)t * p.K + tid;
-      int row = __ldg(p.src2dst + a);
+struct Slots {
+  int row[kBatch];
+  float w[kBatch];
+};
+
+__device__ __forceinline__ void load_slots(const CombineArgs& p, int t, int n_live, int k0,
+                                           Slots& s) {
+#pragma unroll
+  for (int j = 0; j < kBatch; ++j) {
+    const int k = k0 + j;
+    int row = -1;
+    float w = 0.0f;
+    if (t < n_live && k < p.K) {
+      const int64_t a = (int64_t)t * p.K + k;
+      row = __ldg(p.src2dst + a);
       if (row >= 0 && (int64_t)row >= p.R) {
         set_status(p.status, kStBadLayout);
         row = -1;
       }
-      s_row[buf][tid] = row;
-      s_w[buf][tid] = (p.w != nullptr) ? __ldg(p.w + a) : 1.0f;
+      w = (p.w != nullptr) ? __ldg(p.w + a) : 1.0f;
     }
-    __syncthreads();
-    const int* rows = s_row[buf];
-    const float* ws = s_w[buf];
+    s.row[j] = row;
+    s.w[j] = w;
+  }
+}
+
+__global__ void __launch_bounds__(256) combine_kernel(CombineArgs p) {
+  const int tid = threadIdx.x, bd = blockDim.x;
+  const int nch = p.H / 8;
+  const int n_live = live_count(p.d_num_tokens, p.T, p.status, blockIdx.x == 0 && tid == 0);
+  Slots next;
+  load_slots(p, blockIdx.x, n_live, 0, next);
+  for (int t = blockIdx.x; t < n_live; t += gridDim.x) {
+    const Slots first = next;
+    load_slots(p, t + gridDim.x, n_live, 0, next);  // prefetch the next token's slots
     uint16_t* orow = p.out + (int64_t)t * p.H;
     for (int c0 = 0; c0 < nch; c0 += kCPT * bd) {
       float acc[kCPT][8];
@@ -51,25 +66,24 @@ __global__ void __launch_bounds__(512) combine_kernel(CombineArgs p) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
       for (int k0 = 0; k0 < p.K; k0 += kBatch) {
+        Slots s;
+        if (k0 == 0) s = first; else load_slots(p, t, n_live, k0, s);
         uint4 v[kCPT][kBatch];
 #pragma unroll
         for (int j = 0; j < kBatch; ++j) {
-          const int k = k0 + j;
-          const int row = (k < p.K) ? rows[k] : -1;
 #pragma unroll
           for (int i = 0; i < kCPT; ++i) {
             const int c = c0 + i * bd + tid;
-            if (row >= 0 && c < nch)
-              v[i][j] = ld_nc_v4(p.y + (int64_t)row * p.ldy + c * 8);
+            if (s.row[j] >= 0 && c < nch)
+              v[i][j] = ld_nc_v4(p.y + (int64_t)s.row[j] * p.ldy + c * 8);
             else
               v[i][j] = make_uint4(0, 0, 0, 0);
           }
         }
 #pragma unroll
         for (int j = 0; j < kBatch; ++j) {
-          const int k = k0 + j;
-          if (k < p.K && rows[k] >= 0) {
-            const float wk = ws[k];
+          if (s.row[j] >= 0) {
+            const float wk = s.w[j];
 #pragma unroll
             for (int i = 0; i < kCPT; ++i) {
               acc[i][0] = __fmaf_rn(wk, bf16_lo(v[i][j].x), acc[i][0]);
@@ -103,10 +117,13 @@ __global__ void __launch_bounds__(512) combine_kernel(CombineArgs p) {
 }  // namespace
 
 cudaError_t launch_combine(const CombineArgs& a, int num_sms, cudaStream_t s) {
+  // Threads per CTA: enough chunks per thread that a thread covers its share of
+  // the row in about two passes of kCPT chunks; at most 256.
   const int nch = a.H / 8;
-  int bd = (nch + kCPT - 1) / kCPT;
+  int bd = (nch + 2 * kCPT - 1) / (2 * kCPT);
   bd = (bd + 31) / 32 * 32;
-  if (bd > 512) bd = 512;
+  if (bd > 256) bd = 256;
+  if (bd < 32) bd = 32;
   int per_sm = 0;
   cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, combine_kernel, bd, 0);
   if (err != cudaSuccess) return err;

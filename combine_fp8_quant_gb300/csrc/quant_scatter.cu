@@ -117,9 +117,26 @@ __global__ void __launch_bounds__(1024) quant_scatter_kernel(ScatterArgs p) {
   }
 
   // ---- tokens -------------------------------------------------------------
+  // The first pass of a token's x loads is issued before the barrier, so it
+  // overlaps the dependent lookups (id -> rank -> chunk base) of its rows.
   int it = 0;
   for (int t = blockIdx.x; t < n_live; t += gridDim.x, ++it) {
     const int buf = it & 1;
+    const uint16_t* xrow = p.x + (int64_t)t * p.ldx;
+    uint4 v[kCPT][2];
+    auto load_pass = [&](int c0) {
+#pragma unroll
+      for (int i = 0; i < kCPT; ++i) {
+        const int c = c0 + i * bd + tid;
+        if (c < nch) {
+          v[i][0] = ld_nc_v4(xrow + c * 16);
+          v[i][1] = ld_nc_v4(xrow + c * 16 + 8);
+        } else {
+          v[i][0] = v[i][1] = make_uint4(0, 0, 0, 0);
+        }
+      }
+    };
+    load_pass(0);
     if (tid < nslots) {
       const int k = tid;
       int row = -1;
@@ -158,19 +175,8 @@ __global__ void __launch_bounds__(1024) quant_scatter_kernel(ScatterArgs p) {
     }
     __syncthreads();
 
-    const uint16_t* xrow = p.x + (int64_t)t * p.ldx;
     for (int c0 = 0; c0 < nch; c0 += kCPT * bd) {
-      uint4 v[kCPT][2];
-#pragma unroll
-      for (int i = 0; i < kCPT; ++i) {
-        const int c = c0 + i * bd + tid;
-        if (c < nch) {
-          v[i][0] = ld_nc_v4(xrow + c * 16);
-          v[i][1] = ld_nc_v4(xrow + c * 16 + 8);
-        } else {
-          v[i][0] = v[i][1] = make_uint4(0, 0, 0, 0);
-        }
-      }
+      if (c0 > 0) load_pass(c0);
 #pragma unroll
       for (int i = 0; i < kCPT; ++i) {
         const int c = c0 + i * bd + tid;

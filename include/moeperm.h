@@ -148,7 +148,8 @@ size_t moe_workspace_bytes(int32_t T, int32_t K, int32_t L);
  *   block_e                      segment alignment (>= 1), 128 in the sources
  *   g, fmt                       group size and scale layout (pairs above)
  * Outputs (rows of the compact layout, bound = moe_compact_bound(T*K, L, block_e);
- * the caller's buffers must hold at least `bound` rows)
+ * the caller's buffers must hold at least `bound` rows; when bound is 0, i.e.
+ * T = 0, xq / scales / m_indices may be NULL)
  *   xq [bound, H] e4m3           row r = quantised token of the slot that owns r
  *   scales (fmt, ld_s)           scales of the same rows
  *   m_indices [bound] int32      expert id on valid rows, -1 on padding rows and on
@@ -299,8 +300,9 @@ moe_status_t fp8_requant_per_tensor(
 /* ------------------------------------------------------------------ */
 
 /* Waits for `stream`, reads the device status word and returns MOE_OK or the
- * error its lowest set bit names (MOE_ERR_CUDA if the wait or copy fails). The
- * non-graph "fail fast" check of [P3 风险与影响 item 1]. */
+ * most severe error it holds: MOE_ERR_BAD_LAYOUT, then MOE_ERR_LIVE_OVERFLOW,
+ * then MOE_ERR_OVERFLOW (MOE_ERR_CUDA if the wait or copy fails). The non-graph
+ * "fail fast" check of [P3 风险与影响 item 1]. */
 moe_status_t moe_status_sync(const int32_t* d_status, moe_stream_t stream);
 
 /* Static description of a status code. */

@@ -11,11 +11,14 @@ constant with the CUDA library.
 
 Parity pins: every function here is pinned in ``tests/test_oracle_pins.py``
 against the OCP E4M3 specification, closed forms, brute force on tiny inputs,
-library routines, and the constants the SGLang pull-request digests print. The
-choices the sources leave open (row order inside an expert, the zero-group
-exponent, the packed-scale byte order, the per-tensor scale definition) are
-fixed by decision and are "parity unpinned" in that sense; each is listed in
-DESIGN.md.
+library routines, and the constants the SGLang pull-request digests print.
+
+Parity unpinned (fixed by decision because the sources leave them open, so no
+source can confirm them): the row order inside an expert segment (ascending
+t*K + k), the exponent of an all-zero group (from max(amax, 1e-10)), the byte
+order and pad bytes of the packed UE8M0 words (group 4w in the low byte, pads
+zero), and the per-tensor scale of the requant (S = max of the per-token
+scales). Everything downstream of these choices is pinned.
 """
 from __future__ import annotations
 

@@ -493,11 +493,12 @@ def test_repack_bad_layout_flagged(dev, ref):
     st = torch.zeros(1, dtype=torch.int32, device=DEV)
     slab = torch.zeros((L * cap, H), dtype=torch.uint8, device=DEV)
     mm = torch.zeros(L, dtype=torch.int32, device=DEV)
-    for psum in ([3, 2, 9], [3, 6, 20]):
+    for psum in ([3, 2, 9], [3, 6, 20]):   # a negative count; an end past the buffer (+ overflow)
         st.zero_()
         assert dev.moe_expand_to_slab(to_dev(exp), 1, H, 12, None, 0, to_dev(np.array(psum, np.int32)),
                                       L, align, cap, "u8", 128, slab, None, 0, mm, st) == 0
-        assert dev.moe_status_sync(st) == dev.MOE_ERR_BAD_LAYOUT
+        assert dev.moe_status_sync(st) == dev.MOE_ERR_BAD_LAYOUT   # the most severe bit wins
+        assert int(st.item()) & dev.STATUS_BAD_LAYOUT
 
 
 # ---------------------------------------------------------------------------
