@@ -67,6 +67,9 @@ def _declare(L):
                                        vp, vp, i64, vp, i64, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]),
         "moe_dispatch_masked": (i32, [vp, i64, i32, vp, i32, vp, vp, i32, i32, i32, i32, i32, i32,
                                       vp, vp, i64, vp, vp, vp, vp, sz, vp, vp]),
+        "moe_dispatch_compact_noalloc": (i32, [vp, i64, i32, vp, i32, vp, vp, i32, i32, i32, i32,
+                                               i32, i32, vp, vp, i64, vp, i64, vp, vp, vp, vp, vp,
+                                               vp, vp, vp]),
         "moe_quant_group": (i32, [vp, i64, i32, vp, i32, i32, i32, vp, vp, i64, vp, vp]),
         "moe_combine": (i32, [vp, i64, i64, vp, vp, i32, vp, i32, i32, vp, vp, vp]),
         "moe_expand_to_slab": (i32, [vp, i32, i32, i64, vp, i64, vp, i32, i32, i32, i32, i32, vp,
@@ -135,6 +138,19 @@ def moe_dispatch_compact(x, ldx, T, d_num_tokens, H, topk_ids, topk_weights, K, 
         block_e, g, FMT[fmt], _ptr(xq), _ptr(scales), ld_s, _ptr(m_indices), bound,
         _ptr(src2dst), _ptr(counts), _ptr(starts), _ptr(psum), _ptr(total), _ptr(row_weights),
         _ptr(workspace), workspace_bytes, _ptr(d_status), _stream(stream)))
+
+
+def moe_dispatch_compact_noalloc(x, ldx, T, d_num_tokens, H, topk_ids, topk_weights, K, E, L,
+                                 block_e, g, fmt, xq, scales, ld_s, m_indices, bound, src2dst,
+                                 counts, starts, psum, total, row_weights, d_status,
+                                 stream=None) -> int:
+    """moe_dispatch_compact for callers that cannot allocate device memory: the
+    scratch is a static device array inside the library (see the C header)."""
+    return int(lib().moe_dispatch_compact_noalloc(
+        _ptr(x), ldx, T, _ptr(d_num_tokens), H, _ptr(topk_ids), _ptr(topk_weights), K, E, L,
+        block_e, g, FMT[fmt], _ptr(xq), _ptr(scales), ld_s, _ptr(m_indices), bound,
+        _ptr(src2dst), _ptr(counts), _ptr(starts), _ptr(psum), _ptr(total), _ptr(row_weights),
+        _ptr(d_status), _stream(stream)))
 
 
 def moe_dispatch_masked(x, ldx, T, d_num_tokens, H, topk_ids, topk_weights, K, E, L, cap, g,

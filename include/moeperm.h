@@ -175,6 +175,39 @@ moe_status_t moe_dispatch_compact(
     moe_stream_t stream);
 
 /*
+ * moe_dispatch_compact_noalloc -- moe_dispatch_compact without a caller-provided
+ * workspace. The SGLang pages have no counterpart of this call.
+ *
+ * Who it is for: callers that cannot allocate device memory -- code running
+ * while a CUDA graph is captured (allocation is not allowed there), plugins
+ * whose host engine owns every allocation and passes in only inputs and
+ * outputs, and serving loops that forbid allocation after start-up. It calls
+ * no cudaMalloc, cudaFree or other allocating routine.
+ *
+ * Arguments, outputs, results and errors are those of moe_dispatch_compact
+ * without `workspace` / `workspace_bytes`. The scratch lives in one static
+ * device array of 65,792 bytes (64 KiB + 256) that every GPU loading the
+ * library holds until the process exits; a call whose moe_workspace_bytes(T,
+ * K, L) exceeds it returns MOE_ERR_INVALID_ARG before any CUDA call (e.g. the
+ * 8192-token, top-8, 256-expert prefill needs 16,640 bytes).
+ *
+ * - The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.
+ * - Each call enqueues a memset that clears the part of the array it uses,
+ *   then the two dispatch kernels, on `stream`.
+ * - All calls share the one array: calls that can overlap on the GPU (other
+ *   streams, other threads) race on it and must be serialised by the caller.
+ */
+moe_status_t moe_dispatch_compact_noalloc(
+    const void* x, int64_t ldx, int32_t T, const int32_t* d_num_tokens, int32_t H,
+    const int32_t* topk_ids, const float* topk_weights, int32_t K, int32_t E, int32_t L,
+    int32_t block_e, int32_t g, moe_scale_fmt_t fmt,
+    void* xq, void* scales, int64_t ld_s, int32_t* m_indices, int64_t bound,
+    int32_t* src2dst, int32_t* counts, int32_t* starts, int32_t* psum, int32_t* total,
+    float* row_weights, int32_t* d_status, moe_stream_t stream);
+
+/*
  * moe_dispatch_masked -- [P1 实现拆解 item 2-3 (masked path,
  * moe_ep_deepgemm_preprocess), P3 关键源码片段 (masked slab [E_local, max_m,
  * hidden], masked_m = real counts)].
