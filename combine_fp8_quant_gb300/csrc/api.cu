@@ -15,7 +15,8 @@ namespace {
 constexpr int kMaxK = 32;
 constexpr int kMaxL = 1024;
 constexpr int64_t kMaxAssignments = int64_t(1) << 20;
-constexpr size_t kWsHeader = 256;  // ticket word, padded
+constexpr int kMaxHidden = 32768;   // one pass of 2 chunks x 1024 threads per row
+constexpr size_t kWsHeader = 256;  // reserved header before the chunk table
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -63,7 +64,8 @@ moe_status_t check_common(const DispatchCommon& c) {
   if (c.T < 0 || c.H <= 0 || c.H % 16 || (c.g != 32 && c.g != 128) || c.H % c.g) return MOE_ERR_INVALID_ARG;
   if (!fmt_ok(c.fmt, c.g)) return MOE_ERR_INVALID_ARG;
   if (c.K < 1 || c.K > kMaxK || c.L < 1 || c.L > kMaxL || c.E < c.L) return MOE_ERR_INVALID_ARG;
-  if ((int64_t)c.T * c.K > kMaxAssignments) return MOE_ERR_INVALID_ARG;
+  if ((int64_t)c.T * c.K > kMaxAssignments || c.H > kMaxHidden) return MOE_ERR_INVALID_ARG;
+  if (route_plan_S((int64_t)c.T * c.K, c.L) == 0) return MOE_ERR_INVALID_ARG;
   if (c.T > 0) {
     if (!c.x || !aligned16(c.x) || c.ldx < c.H || c.ldx % 8) return MOE_ERR_INVALID_ARG;
     if (!c.ids || !c.src2dst) return MOE_ERR_INVALID_ARG;
@@ -81,30 +83,28 @@ moe_status_t run_dispatch(const DispatchCommon& c, int mode, int32_t block_e, in
   const int sms = num_sms_cached();
   if (sms <= 0) return MOE_ERR_CUDA;
   const int64_t A = (int64_t)c.T * c.K;
-  const int S = route_plan_S(A);
+  const int S = route_plan_S(A, c.L);
   const int64_t nchunks = route_nchunks(A, S);
-  unsigned int* ticket = reinterpret_cast<unsigned int*>(c.ws);
   int32_t* table = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(c.ws) + kWsHeader);
 
   RoutePlanArgs rp{};
   rp.ids = c.ids; rp.d_num_tokens = c.d_num_tokens;
-  rp.T = c.T; rp.K = c.K; rp.L = c.L; rp.mode = mode; rp.block_e = block_e; rp.cap = cap;
+  rp.T = c.T; rp.K = c.K; rp.L = c.L;
   rp.chunk = 256 * S; rp.nchunks = (int32_t)nchunks;
-  rp.lrank = c.src2dst; rp.table = table; rp.ticket = ticket;
-  rp.counts = counts; rp.starts = starts; rp.psum = psum; rp.total = total;
-  rp.masked_m = masked_m; rp.status = d_status;
-  cudaError_t err = launch_route_plan(rp, S, stream);
-  if (err != cudaSuccess) return MOE_ERR_CUDA;
+  rp.lrank = c.src2dst; rp.table = table; rp.status = d_status;
+  if (launch_route_plan(rp, S, stream) != cudaSuccess) return MOE_ERR_CUDA;
 
   ScatterArgs sa{};
   sa.x = static_cast<const uint16_t*>(c.x); sa.ldx = c.ldx; sa.T = c.T;
   sa.d_num_tokens = c.d_num_tokens; sa.H = c.H; sa.ids = c.ids; sa.w = c.w;
-  sa.K = c.K; sa.L = c.L; sa.mode = mode; sa.cap = cap; sa.chunk = rp.chunk; sa.table = table;
+  sa.K = c.K; sa.L = c.L; sa.mode = mode; sa.block_e = block_e; sa.cap = cap;
+  sa.chunk = rp.chunk; sa.nchunks = rp.nchunks; sa.table = table;
   sa.xq = static_cast<uint8_t*>(c.xq); sa.scales = c.scales; sa.ld_s = c.ld_s;
   sa.src2dst = c.src2dst; sa.row_weights = c.row_weights;
-  sa.m_indices = m_indices; sa.bound = bound; sa.starts = starts; sa.psum = psum;
-  sa.status = d_status;
-  return cuda_status(launch_quant_scatter(sa, c.g, c.fmt, sms, stream));
+  sa.m_indices = m_indices; sa.bound = bound;
+  sa.counts = counts; sa.starts = starts; sa.psum = psum; sa.total = total;
+  sa.masked_m = masked_m; sa.status = d_status;
+  return cuda_status(launch_quant_scatter(sa, c.g, c.fmt, sms, /*after_route_plan=*/true, stream));
 }
 
 }  // namespace
@@ -130,7 +130,9 @@ size_t moe_scale_bytes(moe_scale_fmt_t fmt, int64_t rows, int32_t H, int32_t g) 
 size_t moe_workspace_bytes(int32_t T, int32_t K, int32_t L) {
   if (T < 0 || K < 1 || L < 1) return 0;
   const int64_t A = (int64_t)T * K;
-  const int64_t nchunks = route_nchunks(A, route_plan_S(A));
+  const int S = route_plan_S(A, L);
+  if (S == 0) return 0;
+  const int64_t nchunks = route_nchunks(A, S);
   return kWsHeader + (size_t)nchunks * (size_t)L * sizeof(int32_t);
 }
 
@@ -178,7 +180,8 @@ moe_status_t moe_dispatch_masked(
 moe_status_t moe_quant_group(const void* x, int64_t ldx, int32_t T_cap, const int32_t* d_num_live,
                              int32_t H, int32_t g, moe_scale_fmt_t fmt, void* xq, void* scales,
                              int64_t ld_s, int32_t* d_status, moe_stream_t stream) {
-  if (T_cap < 0 || H <= 0 || H % 16 || (g != 32 && g != 128) || H % g || !fmt_ok(fmt, g))
+  if (T_cap < 0 || H <= 0 || H % 16 || H > kMaxHidden || (g != 32 && g != 128) || H % g ||
+      !fmt_ok(fmt, g))
     return MOE_ERR_INVALID_ARG;
   if (T_cap == 0) return MOE_OK;
   if (!x || !aligned16(x) || ldx < H || ldx % 8) return MOE_ERR_INVALID_ARG;
@@ -190,7 +193,8 @@ moe_status_t moe_quant_group(const void* x, int64_t ldx, int32_t T_cap, const in
   sa.x = static_cast<const uint16_t*>(x); sa.ldx = ldx; sa.T = T_cap; sa.d_num_tokens = d_num_live;
   sa.H = H; sa.K = 1; sa.L = 1; sa.mode = kModeIdentity; sa.cap = 0; sa.chunk = 1;
   sa.xq = static_cast<uint8_t*>(xq); sa.scales = scales; sa.ld_s = ld_s; sa.status = d_status;
-  return cuda_status(launch_quant_scatter(sa, g, (int)fmt, sms, reinterpret_cast<cudaStream_t>(stream)));
+  return cuda_status(launch_quant_scatter(sa, g, (int)fmt, sms, /*after_route_plan=*/false,
+                                          reinterpret_cast<cudaStream_t>(stream)));
 }
 
 moe_status_t moe_combine(const void* y, int64_t ldy, int64_t R, const int32_t* src2dst,

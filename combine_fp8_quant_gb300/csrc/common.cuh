@@ -134,6 +134,17 @@ __device__ __forceinline__ void st_v4(void* p, const uint4& v) {
                : "memory");
 }
 
+// Programmatic dependent launch: a primary grid lets its dependent be
+// scheduled early; the dependent waits for the primary's completion (and the
+// visibility of its memory) before touching its results. Both are no-ops for
+// launches without the programmatic attribute.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_primary() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ int64_t align_up64(int64_t c, int64_t b) { return (c + b - 1) / b * b; }
 
 }  // namespace moeperm

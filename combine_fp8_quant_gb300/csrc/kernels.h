@@ -8,30 +8,24 @@
 
 namespace moeperm {
 
+// Largest chunk table (chunks x local experts, int32) a dispatch may use: the
+// scatter launch holds it in shared memory (64 KiB).
+constexpr int kMaxTableInts = 16384;
+
 // ---------------------------------------------------------------------------
-// Route plan: per-chunk expert histograms, stable in-chunk ranks, and (in the
-// last chunk to finish) the per-expert totals, segment starts and the table of
-// per-chunk row bases.
+// Route plan: per-chunk expert histograms and stable in-chunk ranks.
 // ---------------------------------------------------------------------------
 struct RoutePlanArgs {
   const int32_t* ids;          // [T, K]
   const int32_t* d_num_tokens; // optional live tokens
   int32_t T, K, L;
-  int32_t mode;                // kModeCompact / kModeMasked
-  int32_t block_e, cap;
   int32_t chunk;               // assignments per chunk (= 256 * S)
   int32_t nchunks;
   int32_t* lrank;              // [T*K] out: stable rank inside the chunk, -1 dropped
-  int32_t* table;              // [nchunks, L] workspace: chunk histogram -> row base
-  unsigned int* ticket;        // workspace word, zero between calls
-  int32_t* counts;             // [L] compact (may be null for masked)
-  int32_t* starts;             // [L] compact
-  int32_t* psum;               // [L] compact
-  int32_t* total;              // [1] compact
-  int32_t* masked_m;           // [L] masked
+  int32_t* table;              // [nchunks, L] out: chunk histogram
   int32_t* status;
 };
-int route_plan_S(int64_t A);                        // assignments per lane per chunk
+int route_plan_S(int64_t A, int L);                 // 0 if the table cannot fit
 cudaError_t launch_route_plan(const RoutePlanArgs& a, int S, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
@@ -47,9 +41,9 @@ struct ScatterArgs {
   const float* w;
   int32_t K, L;
   int32_t mode;
-  int32_t cap;
-  int32_t chunk;
-  const int32_t* table;
+  int32_t block_e, cap;
+  int32_t chunk, nchunks;
+  const int32_t* table;        // route-plan chunk histograms [nchunks, L]
   uint8_t* xq;
   void* scales;
   int64_t ld_s;
@@ -57,12 +51,15 @@ struct ScatterArgs {
   float* row_weights;
   int32_t* m_indices;          // compact: [bound]
   int64_t bound;
-  const int32_t* starts;       // compact: route-plan outputs used by the m_indices fill
-  const int32_t* psum;
+  int32_t* counts;             // compact outputs [L] (CTA 0 writes them)
+  int32_t* starts;
+  int32_t* psum;
+  int32_t* total;              // [1]
+  int32_t* masked_m;           // masked output [L]
   int32_t* status;
 };
 cudaError_t launch_quant_scatter(const ScatterArgs& a, int g, int fmt, int num_sms,
-                                 cudaStream_t s);
+                                 bool after_route_plan, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
 // Combine

@@ -7,9 +7,8 @@
 //   - plugins hosted by an engine that owns every device allocation and hands
 //     out only inputs and outputs;
 //   - latency-critical serving loops that forbid allocation after start-up.
-// moe_dispatch_compact needs a small scratch workspace (a ticket word and a
-// per-chunk expert table), which such a caller would otherwise have to
-// allocate. This variant keeps that scratch in one file-scope device array of
+// moe_dispatch_compact needs a small scratch workspace (the per-chunk expert
+// table), which such a caller would otherwise have to allocate. This variant keeps that scratch in one file-scope device array of
 // fixed size instead. Every GPU that loads the library holds the array until
 // the process exits.
 //
@@ -17,8 +16,8 @@
 // name is only a host-side stand-in. The address is therefore looked up once
 // per device with cudaGetSymbolAddress, on the first call made with that
 // device current, and cached. Calls after that only enqueue a memset of the
-// used part of the array (so the ticket word starts at zero) and the two
-// dispatch kernels.
+// used part of the array (so no call can see a previous call's table) and the
+// two dispatch kernels.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -28,7 +27,7 @@
 
 namespace {
 
-// 64 KiB chunk table plus the 256-byte header that holds the ticket word.
+// 64 KiB chunk table plus the 256-byte reserved header of the workspace layout.
 constexpr size_t kNoAllocScratchBytes = 64 * 1024 + 256;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 

@@ -1,28 +1,39 @@
-// quant_scatter.cu -- FP8 group quantisation fused with the dispatch scatter.
+// quant_scatter.cu -- FP8 group quantisation fused with the dispatch scatter
+// (second dispatch launch), and the live-row quantiser.
 //
 // What it computes:
 //   * [PR #33128 实现拆解 item 3; PR #36119 实现拆解 item 1] each token row is
 //     quantised ONCE: per group of g elements e = ceil(log2(max(amax,1e-10)/448)),
 //     scale byte e + 127, q = RNE_e4m3(x * 2^-e) -- the power-of-two scale is
 //     chosen directly, never an fp32 scale rounded afterwards;
-//   * the packed row and its scales are then written to the destination row of
-//     every kept (token, slot): compact row = chunk row base + chunk rank,
-//     masked row = e * cap + rank (dropped past cap);
-//   * src2dst is rewritten from chunk ranks to final rows, row weights copied;
+//   * the layout from the route plan's chunk histograms: per expert the count,
+//     compact start[e] = sum_{e'<e} align(count[e'], block_e), psum, total,
+//     masked_m = min(count, cap) and the overflow flag;
+//   * the row of every kept (token, slot): compact start[e] + (slots of e in
+//     earlier chunks) + chunk rank; masked e*cap + rank, dropped past cap;
+//   * the quantised row and its scales written to each of the token's rows;
+//     src2dst rewritten from chunk ranks to rows; row weights copied;
 //   * compact only: m_indices over the whole static bound -- expert id on valid
 //     rows, -1 on padding rows and on the tail [PR #33128 _fwd_kernel_ep_scatter_1].
-//   The identity mode (row t -> row t, K = 1) is the live-row quantiser of
+//   The identity mode (row t -> row t, one slot) is the live-row quantiser of
 //   PR #36119: rows >= the device live count are never touched.
 //
-// Design: a persistent grid (a multiple of the SM count, independent of the
-// routing) walks the live tokens; each CTA owns a token at a time. A thread
-// owns 16-element chunks (two 16-byte loads, one 16-byte e4m3 store per
-// destination); the g/16 lanes of a group reduce the group max with xor
-// shuffles on sign-cleared bf16 bit patterns. All loads of a pass are issued
-// before any math, and every payload store is a full 16-byte vector, so each
-// warp writes 512 contiguous bytes per destination row. Scales: for the packed
-// UE8M0 layout a warp covers exactly one 32-bit word (4 groups of 128), built
-// with shuffles and written once per destination.
+// Design: a persistent grid (SMs x resident CTAs, independent of the routing)
+// walks the live tokens, t = blockIdx.x + i * gridDim.x. One thread owns two
+// 16-element chunks of a row (two 16-byte loads each, one 16-byte e4m3 store
+// per destination), so a single pass covers H <= 32768.
+//   Prologue: the CTA issues its first token's loads, then waits for the route
+//   plan (programmatic dependent launch: this grid is already resident while
+//   the route plan runs), loads the chunk table (<= 64 KiB) into shared memory,
+//   scans it, and resolves the rows of all of its own slots at once. The
+//   route plan therefore needs no serial "last block" and no fence, and the
+//   token loop never waits at a barrier.
+//   Token loop: the next token's loads are issued before the current token's
+//   stores; the g/16 lanes of a group reduce the group max with xor shuffles on
+//   sign-cleared bf16 bit patterns; the exponent comes from the float's bit
+//   fields; conversion is cvt.rn.satfinite.e4m3x2.f32. A warp writes 512
+//   contiguous bytes per destination row, and for the packed UE8M0 layout
+//   exactly one 32-bit scale word (4 groups of 128).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -30,16 +41,14 @@ namespace moeperm {
 
 namespace {
 
-constexpr int kCPT = 2;        // 16-element chunks per thread per pass
-constexpr int kMaxK = 32;
+constexpr int kCPT = 2;  // 16-element chunks per thread
 
 template <int GSZ, int FMT>
-__device__ __forceinline__ void store_scales(const ScatterArgs& p, int nslots,
-                                             const int* s_dst, const int64_t* s_pk,
-                                             int lane, bool active, int e,
-                                             int group_base, int G) {
-  constexpr int GL = GSZ / 16;     // lanes per group
-  constexpr int GPW = 32 / GL;     // groups per warp
+__device__ __forceinline__ void store_scales(const ScatterArgs& p, int nslots, const int* rows,
+                                             int lane, bool active, int e, int group_base,
+                                             int G, int G4) {
+  constexpr int GL = GSZ / 16;  // lanes per group
+  constexpr int GPW = 32 / GL;  // groups per warp
   const uint32_t byte = active ? (uint32_t)(e + 127) : 0u;
   const int gidx = group_base + lane / GL;
   const bool leader = active && (lane % GL) == 0;
@@ -52,11 +61,19 @@ __device__ __forceinline__ void store_scales(const ScatterArgs& p, int nslots,
     if (lane == 0 && active) {
       const int64_t wofs = (int64_t)(group_base / 4) * p.ld_s;
       uint32_t* sc = reinterpret_cast<uint32_t*>(p.scales);
-      for (int k = 0; k < nslots; ++k)
-        if (s_dst[k] >= 0) sc[s_pk[k] + wofs] = word;
+      for (int k = 0; k < nslots; ++k) {
+        const int row = rows[k];
+        if (row < 0) continue;
+        int64_t pk = row;  // compact / identity: one block
+        if (p.mode == kModeMasked) {
+          const int ex = row / p.cap;
+          pk = (int64_t)ex * G4 * p.ld_s + (row - ex * p.cap);
+        }
+        sc[pk + wofs] = word;
+      }
     }
   } else if constexpr (FMT == kFmtU8) {
-    constexpr int WPW = GPW / 4;   // whole 4-group words per warp
+    constexpr int WPW = GPW / 4;  // whole 4-group words per warp
     const int q = lane % WPW;
     uint32_t word = 0;
 #pragma unroll
@@ -65,173 +82,269 @@ __device__ __forceinline__ void store_scales(const ScatterArgs& p, int nslots,
     uint8_t* sc = reinterpret_cast<uint8_t*>(p.scales);
     if (word_ok && lane < WPW && group_base + 4 * q + 3 < G) {
       for (int k = 0; k < nslots; ++k)
-        if (s_dst[k] >= 0)
-          *reinterpret_cast<uint32_t*>(sc + (int64_t)s_dst[k] * p.ld_s + group_base + 4 * q) = word;
+        if (rows[k] >= 0)
+          *reinterpret_cast<uint32_t*>(sc + (int64_t)rows[k] * p.ld_s + group_base + 4 * q) = word;
     }
     const bool by_word = word_ok && ((gidx / 4) * 4 + 3 < G);
     if (leader && !by_word) {
       for (int k = 0; k < nslots; ++k)
-        if (s_dst[k] >= 0) sc[(int64_t)s_dst[k] * p.ld_s + gidx] = (uint8_t)byte;
+        if (rows[k] >= 0) sc[(int64_t)rows[k] * p.ld_s + gidx] = (uint8_t)byte;
     }
   } else {
     if (leader) {
       float* sc = reinterpret_cast<float*>(p.scales);
       const float v = __uint_as_float((uint32_t)(e + 127) << 23);
       for (int k = 0; k < nslots; ++k)
-        if (s_dst[k] >= 0) sc[(int64_t)s_dst[k] * p.ld_s + gidx] = v;
+        if (rows[k] >= 0) sc[(int64_t)rows[k] * p.ld_s + gidx] = v;
     }
+  }
+}
+
+__device__ __forceinline__ void load_row(uint4 (&v)[kCPT][2], const uint16_t* xrow, int nch,
+                                         int bd, int tid) {
+#pragma unroll
+  for (int i = 0; i < kCPT; ++i) {
+    const int c = i * bd + tid;
+    if (xrow != nullptr && c < nch) {
+      v[i][0] = ld_nc_v4(xrow + c * 16);
+      v[i][1] = ld_nc_v4(xrow + c * 16 + 8);
+    } else {
+      v[i][0] = v[i][1] = make_uint4(0, 0, 0, 0);
+    }
+  }
+}
+
+// Layout prologue of a dispatch CTA (see the file comment). Leaves in shared
+// memory: the exclusive per-expert prefix over chunks (tbl), the expert row
+// base (st: compact start, masked 0) and, for compact, psum (ps).
+__device__ void layout_prologue(const ScatterArgs& p, int32_t* tbl, int32_t* st, int32_t* ps,
+                                int32_t* s_wsum) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, bd = blockDim.x;
+  const int L = p.L, NC = p.nchunks;
+  for (int i = tid; i < NC * L; i += bd) tbl[i] = __ldcg(p.table + i);
+  __syncthreads();
+  for (int e = tid; e < L; e += bd) {
+    int run = 0;
+    for (int c = 0; c < NC; ++c) {
+      const int h = tbl[c * L + e];
+      tbl[c * L + e] = run;
+      run += h;
+    }
+    ps[e] = run;  // count, for now
+  }
+  __syncthreads();
+  if (p.mode == kModeCompact) {
+    // exclusive scan of align(count) over experts; thread i owns a contiguous run
+    const int b = p.block_e;
+    const int per = (L + bd - 1) / bd;
+    const int lo = min(tid * per, L), hi = min(lo + per, L);
+    int local = 0;
+    for (int e = lo; e < hi; ++e) local += (ps[e] + b - 1) / b * b;
+    int incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int nb = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += nb;
+    }
+    if (lane == 31) s_wsum[warp] = incl;
+    __syncthreads();
+    int wbase = 0, total = 0;
+    for (int w = 0; w < (bd >> 5); ++w) {
+      if (w < warp) wbase += s_wsum[w];
+      total += s_wsum[w];
+    }
+    int run = wbase + incl - local;
+    for (int e = lo; e < hi; ++e) {
+      const int cnt = ps[e];
+      st[e] = run;
+      ps[e] = run + cnt;
+      run += (cnt + b - 1) / b * b;
+    }
+    if (blockIdx.x == 0 && tid == 0) *p.total = total;
+    __syncthreads();
+    if (blockIdx.x == 0) {
+      for (int e = tid; e < L; e += bd) {
+        p.counts[e] = ps[e] - st[e];
+        p.starts[e] = st[e];
+        p.psum[e] = ps[e];
+      }
+    }
+  } else {
+    bool overflow = false;
+    for (int e = tid; e < L; e += bd) {
+      const int cnt = ps[e];
+      if (blockIdx.x == 0) p.masked_m[e] = min(cnt, p.cap);
+      if (cnt > p.cap) overflow = true;
+      st[e] = 0;
+    }
+    if (overflow && blockIdx.x == 0) set_status(p.status, kStOverflow);
+    __syncthreads();
   }
 }
 
 template <int GSZ, int FMT>
 __global__ void __launch_bounds__(1024) quant_scatter_kernel(ScatterArgs p) {
-  extern __shared__ int32_t s_geo[];  // compact: [2*L] starts, psum
-  __shared__ int s_dst[2][kMaxK];
-  __shared__ int64_t s_pk[2][kMaxK];
-  const int tid = threadIdx.x, lane = tid & 31;
-  const int bd = blockDim.x;
+  extern __shared__ int32_t sm[];
+  __shared__ int32_t s_wsum[32];
+  const int tid = threadIdx.x, lane = tid & 31, bd = blockDim.x;
   const int H = p.H;
   const int nch = H / 16;
   const int G = H / GSZ;
   const int G4 = (G + 3) / 4;
-  const int nslots = (p.mode == kModeIdentity) ? 1 : p.K;
+  const bool identity = p.mode == kModeIdentity;
+  const int nslots = identity ? 1 : p.K;
   const int n_live = live_count(p.d_num_tokens, p.T, p.status,
-                                p.mode == kModeIdentity && blockIdx.x == 0 && tid == 0);
+                                identity && blockIdx.x == 0 && tid == 0);
 
-  // ---- compact: m_indices over [0, bound) --------------------------------
-  if (p.mode == kModeCompact && p.m_indices != nullptr) {
+  // first token's loads go out before anything waits
+  uint4 v[kCPT][2];
+  load_row(v, (int)blockIdx.x < n_live ? p.x + (int64_t)blockIdx.x * p.ldx : nullptr, nch, bd, tid);
+
+  const int ntok =
+      n_live > (int)blockIdx.x ? (n_live - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  int32_t* rows_s = sm;  // identity mode: unused
+  if (!identity) {
+    pdl_wait_primary();
     const int L = p.L;
-    for (int i = tid; i < L; i += bd) {
-      s_geo[i] = p.starts[i];
-      s_geo[L + i] = p.psum[i];
+    int32_t* tbl = sm;
+    int32_t* st = tbl + p.nchunks * L;
+    int32_t* ps = st + L;
+    rows_s = ps + L;
+    layout_prologue(p, tbl, st, ps, s_wsum);
+
+    if (p.mode == kModeCompact && p.m_indices != nullptr) {
+      for (int64_t r = (int64_t)blockIdx.x * bd + tid; r < p.bound; r += (int64_t)gridDim.x * bd) {
+        int lo = 0, hi = L - 1;  // largest e with start[e] <= r (start[0] = 0)
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (st[mid] <= r) lo = mid; else hi = mid - 1;
+        }
+        p.m_indices[r] = (r < ps[lo]) ? lo : -1;
+      }
+    }
+
+    // rows of every slot this CTA will scatter
+    for (int i = tid; i < ntok * p.K; i += bd) {
+      const int t = blockIdx.x + (i / p.K) * gridDim.x;
+      const int64_t a = (int64_t)t * p.K + (i % p.K);
+      const int e = __ldg(p.ids + a);
+      int row = -1;
+      if (e >= 0 && e < L) {
+        const int lr = p.src2dst[a];
+        const int base = tbl[(int)(a / p.chunk) * L + e];
+        if (p.mode == kModeCompact) {
+          row = st[e] + base + lr;
+          if (lr < 0 || row < 0 || (int64_t)row >= p.bound) {  // never write outside the buffer
+            set_status(p.status, kStBadLayout);
+            row = -1;
+          }
+        } else {
+          const int j = base + lr;
+          if (lr < 0 || j < 0) set_status(p.status, kStBadLayout);
+          else if (j < p.cap) row = e * p.cap + j;
+        }
+      }
+      p.src2dst[a] = row;
+      if (row >= 0 && p.row_weights != nullptr) p.row_weights[row] = __ldg(p.w + a);
+      rows_s[i] = row;
     }
     __syncthreads();
-    for (int64_t r = (int64_t)blockIdx.x * bd + tid; r < p.bound; r += (int64_t)gridDim.x * bd) {
-      int lo = 0, hi = L - 1;  // largest e with starts[e] <= r (starts[0] = 0)
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (s_geo[mid] <= r) lo = mid; else hi = mid - 1;
-      }
-      p.m_indices[r] = (r < s_geo[L + lo]) ? lo : -1;
-    }
   }
 
-  // ---- tokens -------------------------------------------------------------
-  // The first pass of a token's x loads is issued before the barrier, so it
-  // overlaps the dependent lookups (id -> rank -> chunk base) of its rows.
-  int it = 0;
-  for (int t = blockIdx.x; t < n_live; t += gridDim.x, ++it) {
-    const int buf = it & 1;
-    const uint16_t* xrow = p.x + (int64_t)t * p.ldx;
-    uint4 v[kCPT][2];
-    auto load_pass = [&](int c0) {
-#pragma unroll
-      for (int i = 0; i < kCPT; ++i) {
-        const int c = c0 + i * bd + tid;
-        if (c < nch) {
-          v[i][0] = ld_nc_v4(xrow + c * 16);
-          v[i][1] = ld_nc_v4(xrow + c * 16 + 8);
-        } else {
-          v[i][0] = v[i][1] = make_uint4(0, 0, 0, 0);
-        }
-      }
-    };
-    load_pass(0);
-    if (tid < nslots) {
-      const int k = tid;
-      int row = -1;
-      int64_t pk = 0;
-      if (p.mode == kModeIdentity) {
-        row = t;
-        pk = t;
-      } else {
-        const int64_t a = (int64_t)t * p.K + k;
-        const int e = __ldg(p.ids + a);
-        if (e >= 0 && e < p.L) {
-          const int lr = p.src2dst[a];
-          const int b = __ldcg(p.table + (a / p.chunk) * p.L + e);
-          if (p.mode == kModeCompact) {
-            row = b + lr;
-            if (lr < 0 || row < 0 || (int64_t)row >= p.bound) {  // never write outside the buffer
-              set_status(p.status, kStBadLayout);
-              row = -1;
-            }
-            pk = row;
-          } else {
-            const int j = b + lr;
-            if (lr < 0 || j < 0) {
-              set_status(p.status, kStBadLayout);
-            } else if (j < p.cap) {
-              row = e * p.cap + j;
-              pk = (int64_t)e * G4 * p.ld_s + j;
-            }
-          }
-        }
-        p.src2dst[a] = row;
-        if (row >= 0 && p.row_weights != nullptr) p.row_weights[row] = __ldg(p.w + a);
-      }
-      s_dst[buf][k] = row;
-      s_pk[buf][k] = pk;
+  // ---- token loop: no barriers ---------------------------------------------
+  int ident_row[1];
+  for (int it = 0; it < ntok; ++it) {
+    const int t = blockIdx.x + it * gridDim.x;
+    uint4 vn[kCPT][2];
+    const int tn = t + gridDim.x;
+    load_row(vn, tn < n_live ? p.x + (int64_t)tn * p.ldx : nullptr, nch, bd, tid);
+    const int* rows;
+    if (identity) {
+      ident_row[0] = t;
+      rows = ident_row;
+    } else {
+      rows = rows_s + it * p.K;
     }
-    __syncthreads();
-
-    for (int c0 = 0; c0 < nch; c0 += kCPT * bd) {
-      if (c0 > 0) load_pass(c0);
 #pragma unroll
-      for (int i = 0; i < kCPT; ++i) {
-        const int c = c0 + i * bd + tid;
-        const bool active = c < nch;
-        uint32_t m = amax16_bf16(v[i][0], v[i][1]);
+    for (int i = 0; i < kCPT; ++i) {
+      const int c = i * bd + tid;
+      const bool active = c < nch;
+      uint32_t m = amax16_bf16(v[i][0], v[i][1]);
 #pragma unroll
-        for (int off = 1; off < GSZ / 16; off <<= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
-        const int e = group_exponent(__uint_as_float(m << 16));
-        const float inv = exp2_neg(e);
-        const uint2 q0 = quant8(v[i][0], inv), q1 = quant8(v[i][1], inv);
-        const uint4 q = make_uint4(q0.x, q0.y, q1.x, q1.y);
-        if (active) {
-          for (int k = 0; k < nslots; ++k) {
-            const int row = s_dst[buf][k];
-            if (row >= 0) st_v4(p.xq + (int64_t)row * H + c * 16, q);
-          }
+      for (int off = 1; off < GSZ / 16; off <<= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
+      const int e = group_exponent(__uint_as_float(m << 16));
+      const float inv = exp2_neg(e);
+      const uint2 q0 = quant8(v[i][0], inv), q1 = quant8(v[i][1], inv);
+      const uint4 q = make_uint4(q0.x, q0.y, q1.x, q1.y);
+      if (active) {
+        for (int k = 0; k < nslots; ++k) {
+          const int row = rows[k];
+          if (row >= 0) st_v4(p.xq + (int64_t)row * H + c * 16, q);
         }
-        const int cw = c0 + i * bd + (tid & ~31);  // first chunk of this warp
-        if (cw < nch)
-          store_scales<GSZ, FMT>(p, nslots, s_dst[buf], s_pk[buf], lane, active, e,
-                                 cw * 16 / GSZ, G);
       }
+      const int cw = i * bd + (tid & ~31);  // first chunk of this warp
+      if (cw < nch)
+        store_scales<GSZ, FMT>(p, nslots, rows, lane, active, e, cw * 16 / GSZ, G, G4);
+    }
+#pragma unroll
+    for (int i = 0; i < kCPT; ++i) {
+      v[i][0] = vn[i][0];
+      v[i][1] = vn[i][1];
     }
   }
 }
 
 template <int GSZ, int FMT>
-cudaError_t launch_one(const ScatterArgs& a, int num_sms, cudaStream_t s) {
+cudaError_t launch_one(const ScatterArgs& a, int num_sms, bool pdl, cudaStream_t s) {
   const int nch = a.H / 16;
   int bd = (nch + kCPT - 1) / kCPT;
   bd = (bd + 31) / 32 * 32;
-  if (bd > 1024) bd = 1024;
-  const size_t smem = (a.mode == kModeCompact) ? (size_t)2 * a.L * sizeof(int32_t) : 0;
+  if (bd > 1024) return cudaErrorInvalidValue;  // H > 32768 is rejected on the host
+  size_t fixed = 0, per_token = 0;
+  if (a.mode != kModeIdentity) {
+    fixed = ((size_t)a.nchunks * a.L + 2 * (size_t)a.L) * sizeof(int32_t);
+    per_token = (size_t)a.K * sizeof(int32_t);
+  }
+  // Resident CTAs per SM with a provisional row buffer of 8 tokens per CTA;
+  // the grid is then fixed and the row buffer sized for ceil(T / grid) tokens.
   int per_sm = 0;
   cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      &per_sm, quant_scatter_kernel<GSZ, FMT>, bd, smem);
+      &per_sm, quant_scatter_kernel<GSZ, FMT>, bd, fixed + 8 * per_token);
   if (err != cudaSuccess) return err;
   if (per_sm < 1) per_sm = 1;
   int64_t grid = (int64_t)num_sms * per_sm;
   if (grid > a.T) grid = a.T;
   if (grid < 1) grid = 1;
-  quant_scatter_kernel<GSZ, FMT><<<(unsigned)grid, bd, smem, s>>>(a);
-  return cudaGetLastError();
+  const int64_t ntok_max = (a.T + grid - 1) / grid;
+  const size_t smem = fixed + (size_t)ntok_max * per_token;
+  if (smem > 48 * 1024) {
+    err = cudaFuncSetAttribute(quant_scatter_kernel<GSZ, FMT>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(bd);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, quant_scatter_kernel<GSZ, FMT>, a);
 }
 
 }  // namespace
 
 cudaError_t launch_quant_scatter(const ScatterArgs& a, int g, int fmt, int num_sms,
-                                 cudaStream_t s) {
+                                 bool after_route_plan, cudaStream_t s) {
   if (g == 128) {
-    if (fmt == kFmtPacked) return launch_one<128, kFmtPacked>(a, num_sms, s);
-    if (fmt == kFmtU8) return launch_one<128, kFmtU8>(a, num_sms, s);
-    return launch_one<128, kFmtF32>(a, num_sms, s);
+    if (fmt == kFmtPacked) return launch_one<128, kFmtPacked>(a, num_sms, after_route_plan, s);
+    if (fmt == kFmtU8) return launch_one<128, kFmtU8>(a, num_sms, after_route_plan, s);
+    return launch_one<128, kFmtF32>(a, num_sms, after_route_plan, s);
   }
-  return launch_one<32, kFmtU8>(a, num_sms, s);
+  return launch_one<32, kFmtU8>(a, num_sms, after_route_plan, s);
 }
 
 }  // namespace moeperm

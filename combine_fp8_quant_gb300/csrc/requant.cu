@@ -27,11 +27,21 @@ __device__ __forceinline__ uint32_t requant4(uint32_t w, float r) {
          (cvt_e4m3x2(__fmul_rn(b.x, r), __fmul_rn(b.y, r)) << 16);
 }
 
-__global__ void __launch_bounds__(kThreads) requant_kernel(RequantArgs p) {
-  __shared__ float s_red[kThreads / 32];
+__device__ __forceinline__ float block_max_scales(const RequantArgs& p, float* s_red) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   float m = 0.0f;
-  for (int t = tid; t < p.T; t += kThreads) m = fmaxf(m, __ldg(p.s_tok + t));
+  const int T4 = p.T / 4;
+  const bool vec = (reinterpret_cast<uintptr_t>(p.s_tok) & 15u) == 0;
+  if (vec) {
+    const float4* s4 = reinterpret_cast<const float4*>(p.s_tok);
+    for (int i = tid; i < T4; i += kThreads) {
+      const float4 v = __ldg(s4 + i);
+      m = fmaxf(fmaxf(m, fmaxf(v.x, v.y)), fmaxf(v.z, v.w));
+    }
+    for (int t = 4 * T4 + tid; t < p.T; t += kThreads) m = fmaxf(m, __ldg(p.s_tok + t));
+  } else {
+    for (int t = tid; t < p.T; t += kThreads) m = fmaxf(m, __ldg(p.s_tok + t));
+  }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
   if (lane == 0) s_red[warp] = m;
@@ -39,23 +49,49 @@ __global__ void __launch_bounds__(kThreads) requant_kernel(RequantArgs p) {
   float S = 0.0f;
 #pragma unroll
   for (int w = 0; w < kThreads / 32; ++w) S = fmaxf(S, s_red[w]);
+  return S;
+}
+
+__global__ void __launch_bounds__(kThreads) requant_kernel(RequantArgs p) {
+  __shared__ float s_red[kThreads / 32];
+  const int tid = threadIdx.x;
+  const int nch = p.H / 16;
+  // The CTA's first row is loaded before the scale reduction so the two
+  // latencies overlap; every row after that streams with two vectors in flight
+  // per thread.
+  int t = blockIdx.x;
+  uint4 a = make_uint4(0, 0, 0, 0), b = make_uint4(0, 0, 0, 0);
+  if (t < p.T) {
+    const uint8_t* src = p.q + (int64_t)t * p.ldq;
+    if (tid < nch) a = ld_nc_v4(src + (int64_t)tid * 16);
+    if (tid + kThreads < nch) b = ld_nc_v4(src + (int64_t)(tid + kThreads) * 16);
+  }
+  const float S = block_max_scales(p, s_red);
   if (blockIdx.x == 0 && tid == 0) *p.scale_out = (S > 0.0f) ? S : 1.0f;
 
-  const int nch = p.H / 16;
-  for (int t = blockIdx.x; t < p.T; t += gridDim.x) {
+  for (; t < p.T; t += gridDim.x) {
     const float r = (S > 0.0f) ? __fdiv_rn(__ldg(p.s_tok + t), S) : 0.0f;
     const uint8_t* src = p.q + (int64_t)t * p.ldq;
     uint8_t* dst = p.q_out + (int64_t)t * p.H;
     for (int c = tid; c < nch; c += 2 * kThreads) {
       const int c2 = c + kThreads;
-      const uint4 a = ld_nc_v4(src + (int64_t)c * 16);
-      uint4 b = make_uint4(0, 0, 0, 0);
-      if (c2 < nch) b = ld_nc_v4(src + (int64_t)c2 * 16);
+      if (c > tid) {  // passes after the first: load here (the first pass was preloaded)
+        a = ld_nc_v4(src + (int64_t)c * 16);
+        b = (c2 < nch) ? ld_nc_v4(src + (int64_t)c2 * 16) : make_uint4(0, 0, 0, 0);
+      }
       st_v4(dst + (int64_t)c * 16,
             make_uint4(requant4(a.x, r), requant4(a.y, r), requant4(a.z, r), requant4(a.w, r)));
       if (c2 < nch)
         st_v4(dst + (int64_t)c2 * 16,
               make_uint4(requant4(b.x, r), requant4(b.y, r), requant4(b.z, r), requant4(b.w, r)));
+    }
+    // preload the first pass of this CTA's next row
+    const int tn = t + gridDim.x;
+    if (tn < p.T) {
+      const uint8_t* nsrc = p.q + (int64_t)tn * p.ldq;
+      a = (tid < nch) ? ld_nc_v4(nsrc + (int64_t)tid * 16) : make_uint4(0, 0, 0, 0);
+      b = (tid + kThreads < nch) ? ld_nc_v4(nsrc + (int64_t)(tid + kThreads) * 16)
+                                 : make_uint4(0, 0, 0, 0);
     }
   }
 }

@@ -1,30 +1,24 @@
-// route_plan.cu -- expert histogram, stable ranks and prefix sums for the
-// compact and masked dispatch layouts.
+// route_plan.cu -- expert histogram and stable ranks for the compact and
+// masked dispatch layouts (first of the two dispatch launches).
 //
 // What it computes (PR #33128 实现拆解 items 2-3 and code excerpts
 // _get_compact_all_tokens / _fwd_kernel_ep_scatter_1; PR #29525 _build_layout):
-//   count[e]  = kept slots routed to local expert e (ids outside [0, L) dropped)
-//   rank(a)   = kept slots a' < a with the same expert (rows follow t*K + k)
-//   compact:  start[e] = sum_{e'<e} align(count[e'], block_e),
-//             psum[e] = start[e] + count[e], total = sum align(count)
-//   masked:   masked_m[e] = min(count[e], cap), overflow when count[e] > cap
+//   kept slot   a = t*K + k of a live token with 0 <= id < L (others dropped)
+//   table[c][e] = kept slots of chunk c routed to expert e
+//   lrank[a]    = kept slots a' < a of the same chunk with the same expert
+// The prefix sums over chunks and experts (segment starts, psum, total,
+// masked_m) are formed from this table by every CTA of the scatter launch.
 //
-// Design (one launch, fixed grid of `nchunks` CTAs of 8 warps):
-//   * CTA c owns assignments [c*chunk, (c+1)*chunk); warp w owns a contiguous
-//     sub-range of 32*S of them, walked in steps of 32 in order. In a step,
-//     __match_any_sync groups the lanes with the same expert; a lane's rank
-//     among them is the popcount of the lower peers, and the lowest peer adds
-//     the group size to the warp's per-expert counter in shared memory. This
-//     gives a deterministic, stable rank without global atomics.
-//   * The 8 per-warp histograms are scanned per expert into warp bases, the
-//     CTA's total histogram goes to the workspace table, and each slot's rank
-//     inside the chunk is written to `lrank` (the caller's src2dst buffer,
-//     rewritten with final rows by the scatter kernel).
-//   * The last CTA to finish (a ticket taken with atomicInc after a
-//     __threadfence, so no CTA ever waits for another) scans the table: per
-//     expert an exclusive sum over chunks (the chunk's row base), the expert
-//     totals, and a block-wide exclusive scan of the aligned counts. The
-//     ticket wraps back to zero, so the workspace is ready for the next call.
+// Design (fixed grid of `nchunks` CTAs of 8 warps): CTA c owns slots
+// [c*chunk, (c+1)*chunk); warp w owns a contiguous sub-range of 32*S of them,
+// walked in order in steps of 32. In a step, ballots over the bits of the
+// expert id group the lanes with the same expert; a lane's rank among them is
+// the popcount of its lower peers, and the lowest peer adds the group size to
+// the warp's per-expert counter in shared memory. A per-expert scan over the 8 warps turns the
+// warp-local ranks into chunk-local ones. Deterministic and stable, with no
+// global atomics. The CTA signals the dependent scatter launch at its start,
+// so that launch is scheduled while this one runs (it waits for this grid's
+// results before reading them).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -34,12 +28,12 @@ namespace {
 
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
+constexpr int kGroup = 8;  // steps whose peer masks are formed together
 
 template <int S>
 __global__ void __launch_bounds__(kThreads) route_plan_kernel(RoutePlanArgs p) {
   extern __shared__ int32_t smem[];  // [kWarps][L] per-warp histograms
-  __shared__ int s_last;
-  __shared__ int32_t s_wsum[kWarps];
+  pdl_launch_dependents();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int L = p.L;
 
@@ -47,10 +41,6 @@ __global__ void __launch_bounds__(kThreads) route_plan_kernel(RoutePlanArgs p) {
   const int n_live = live_count(p.d_num_tokens, p.T, p.status, blockIdx.x == 0 && tid == 0);
   const int64_t A = (int64_t)p.T * p.K;
   const int64_t A_live = (int64_t)n_live * p.K;
-  __syncthreads();
-
-  // --- stable ranks inside the warp's sub-range ---------------------------
-  int32_t* myhw = smem + warp * L;
   const int64_t base = (int64_t)blockIdx.x * p.chunk + (int64_t)warp * (32 * S);
   int32_t v[S];  // the slot's expert id, then (rank << 11) | (expert + 1); 0 = dropped
 #pragma unroll
@@ -58,23 +48,48 @@ __global__ void __launch_bounds__(kThreads) route_plan_kernel(RoutePlanArgs p) {
     const int64_t a = base + i * 32 + lane;
     v[i] = (a < A_live) ? __ldg(p.ids + a) : -1;
   }
+  __syncthreads();
+
+  // Lanes with the same expert ("peers") are found with one ballot per bit of
+  // the expert id: a lane keeps the lanes that agree with it on every bit.
+  // The masks of 8 steps are formed first (independent), then the per-warp
+  // counters are advanced step by step in order, which fixes a stable rank.
+  int32_t* myhw = smem + warp * L;
   const unsigned lt_mask = (1u << lane) - 1u;
+  const int nbits = (L > 1) ? 32 - __clz(L - 1) : 0;
 #pragma unroll
-  for (int i = 0; i < S; ++i) {
-    int e = v[i];
-    if (e < 0 || e >= L) e = -1;
-    const unsigned peers = __match_any_sync(0xffffffffu, e);
-    const int lower = __popc(peers & lt_mask);
-    int rank = 0;
-    if (e >= 0) rank = myhw[e] + lower;
-    __syncwarp();
-    if (e >= 0 && lower == 0) myhw[e] += __popc(peers);
-    __syncwarp();
-    v[i] = (e >= 0) ? ((rank << 11) | (e + 1)) : 0;
+  for (int i0 = 0; i0 < S; i0 += kGroup) {
+    unsigned peers[kGroup];
+#pragma unroll
+    for (int j = 0; j < kGroup; ++j) {
+      if (i0 + j >= S) break;
+      int e = v[i0 + j];
+      if (e < 0 || e >= L) e = -1;
+      v[i0 + j] = e;
+      unsigned m = __ballot_sync(0xffffffffu, e >= 0);
+      for (int b = 0; b < nbits; ++b) {
+        const unsigned bit = (unsigned)(e >> b) & 1u;
+        const unsigned bal = __ballot_sync(0xffffffffu, bit);
+        m &= bit ? bal : ~bal;
+      }
+      peers[j] = (e >= 0) ? m : 0u;
+    }
+#pragma unroll
+    for (int j = 0; j < kGroup; ++j) {
+      if (i0 + j >= S) break;
+      const int e = v[i0 + j];
+      const int lower = __popc(peers[j] & lt_mask);
+      int rank = 0;
+      if (e >= 0) rank = myhw[e] + lower;
+      __syncwarp();
+      if (e >= 0 && lower == 0) myhw[e] += __popc(peers[j]);
+      __syncwarp();
+      v[i0 + j] = (e >= 0) ? ((rank << 11) | (e + 1)) : 0;
+    }
   }
   __syncthreads();
 
-  // --- per-expert scan over the warps; chunk histogram to the table -------
+  // per-expert exclusive scan over the warps; chunk histogram to the table
   for (int e = tid; e < L; e += kThreads) {
     int run = 0;
 #pragma unroll
@@ -94,90 +109,24 @@ __global__ void __launch_bounds__(kThreads) route_plan_kernel(RoutePlanArgs p) {
       p.lrank[a] = pk ? (myhw[(pk & 0x7FF) - 1] + (pk >> 11)) : -1;
     }
   }
-
-  // --- last CTA: prefix sums over chunks and experts ----------------------
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    const unsigned t = atomicInc(p.ticket, (unsigned)(p.nchunks - 1));
-    s_last = (t == (unsigned)(p.nchunks - 1));
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-
-  int32_t* s_cnt = smem;        // [L] counts
-  int32_t* s_start = smem + L;  // [L] row base of each expert
-  const int NC = p.nchunks;
-  for (int e = tid; e < L; e += kThreads) {
-    int sum = 0;
-#pragma unroll 16
-    for (int c = 0; c < NC; ++c) sum += __ldcg(p.table + (int64_t)c * L + e);
-    s_cnt[e] = sum;
-  }
-  __syncthreads();
-
-  if (p.mode == kModeCompact) {
-    // exclusive scan of align(count) over experts; thread i owns a contiguous run
-    const int per = (L + kThreads - 1) / kThreads;
-    const int lo = min(tid * per, L), hi = min(lo + per, L);
-    const int b = p.block_e;
-    int local = 0;
-    for (int e = lo; e < hi; ++e) local += (s_cnt[e] + b - 1) / b * b;
-    int incl = local;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int nb = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += nb;
-    }
-    if (lane == 31) s_wsum[warp] = incl;
-    __syncthreads();
-    int wbase = 0;
-    for (int w = 0; w < warp; ++w) wbase += s_wsum[w];
-    int run = wbase + incl - local;
-    for (int e = lo; e < hi; ++e) {
-      s_start[e] = run;
-      run += (s_cnt[e] + b - 1) / b * b;
-    }
-    if (tid == kThreads - 1) *p.total = run;
-    __syncthreads();
-  } else {
-    for (int e = tid; e < L; e += kThreads) s_start[e] = 0;
-    __syncthreads();
-  }
-
-  bool overflow = false;
-  for (int e = tid; e < L; e += kThreads) {
-    const int cnt = s_cnt[e];
-    const int st = s_start[e];
-    int run = st;
-#pragma unroll 16
-    for (int c = 0; c < NC; ++c) {
-      int32_t* cell = p.table + (int64_t)c * L + e;
-      const int h = __ldcg(cell);
-      *cell = run;
-      run += h;
-    }
-    if (p.mode == kModeCompact) {
-      p.counts[e] = cnt;
-      p.starts[e] = st;
-      p.psum[e] = st + cnt;
-    } else {
-      p.masked_m[e] = min(cnt, p.cap);
-      if (cnt > p.cap) overflow = true;
-    }
-  }
-  if (overflow) set_status(p.status, kStOverflow);
 }
 
 }  // namespace
 
-int route_plan_S(int64_t A) {
-  // Smallest S with at most 16 chunks; S = 64 allows up to 64 chunks (A <= 2^20).
-  const int cand[] = {1, 4, 16};
-  for (int S : cand)
-    if ((A + (int64_t)kThreads * S - 1) / ((int64_t)kThreads * S) <= 16) return S;
-  return 64;
+int route_plan_S(int64_t A, int L) {
+  // Smallest S whose chunk table fits kMaxTableInts (the scatter launch holds
+  // it in shared memory), preferring at most 16 chunks (a smaller table for
+  // every scatter CTA to scan).
+  const int cand[] = {1, 4, 16, 64};
+  for (int S : cand) {
+    const int64_t nc = (A + (int64_t)kThreads * S - 1) / ((int64_t)kThreads * S);
+    if (nc <= 16 && nc * L <= kMaxTableInts) return S;
+  }
+  for (int S : cand) {
+    const int64_t nc = (A + (int64_t)kThreads * S - 1) / ((int64_t)kThreads * S);
+    if (nc * L <= kMaxTableInts) return S;
+  }
+  return 0;  // too large for one call
 }
 
 cudaError_t launch_route_plan(const RoutePlanArgs& a, int S, cudaStream_t s) {

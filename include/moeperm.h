@@ -119,9 +119,11 @@ int32_t moe_should_use_masked(int32_t E, int32_t L);
 size_t moe_scale_bytes(moe_scale_fmt_t fmt, int64_t rows, int32_t H, int32_t g);
 
 /* Bytes of device workspace the dispatch calls need for T tokens, K slots and L
- * local experts. The workspace must be zero-filled once before its first use;
- * every dispatch call leaves it ready for the next (its ticket word returns to
- * zero). One workspace must not be used by two calls that can run at once. */
+ * local experts: a 256-byte reserved header and the [chunks, L] int32 table of
+ * per-chunk expert histograms (at most 64 KiB; larger T*K x L combinations are
+ * rejected, and this returns 0 for them). The workspace needs no
+ * initialisation. One workspace must not be used by two calls that can run at
+ * once. */
 size_t moe_workspace_bytes(int32_t T, int32_t K, int32_t L);
 
 /* ------------------------------------------------------------------ */
@@ -162,8 +164,12 @@ size_t moe_workspace_bytes(int32_t T, int32_t K, int32_t L);
  * Rows of an expert follow ascending t*K + k (a deterministic, stable order).
  * The segment of expert e is [starts[e], starts[e] + align(counts[e])); starts
  * are the exclusive prefix sums of the aligned counts.
- * Workspace: moe_workspace_bytes(T, K, L) bytes, zero-filled before first use.
- * Launches: 2 (route plan; quantise + scatter + m_indices), fixed grids.
+ * Limits: T*K <= 2^20, H <= 32768, and the chunk table within 64 KiB.
+ * Workspace: moe_workspace_bytes(T, K, L) bytes (no initialisation needed).
+ * Launches: 2, fixed grids -- the route plan (chunk histograms and stable
+ * ranks), then the layout + quantise + scatter + m_indices launch, which is
+ * started early with programmatic dependent launch and waits for the route
+ * plan's results on the device.
  */
 moe_status_t moe_dispatch_compact(
     const void* x, int64_t ldx, int32_t T, const int32_t* d_num_tokens, int32_t H,

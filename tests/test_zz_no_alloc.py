@@ -66,8 +66,10 @@ def test_noalloc_matches_workspace_dispatch_two_calls(dev):
 
 
 def test_noalloc_rejects_sizes_beyond_its_array(dev):
-    T, H, K, L = 40000, 128, 8, 1024          # 20 chunks x 1024 experts: 80 KiB of table
-    assert dev.moe_workspace_bytes(T, K, L) > 64 * 1024 + 256
+    # 20 chunks x 1024 experts would need an 80 KiB table: beyond the array
+    # (and beyond what the dispatch supports at all, so the workspace query says 0)
+    T, H, K, L = 40000, 128, 8, 1024
+    assert dev.moe_workspace_bytes(T, K, L) == 0
     fake = 1 << 20
     code = dev.moe_dispatch_compact_noalloc(fake, H, T, None, H, fake, None, K, L, L, 128, 128,
                                             "packed", fake, fake, 1 << 20, fake, 1 << 22, fake,
