@@ -34,8 +34,8 @@ int num_sms_cached() {
 
 bool fmt_ok(int fmt, int g) {
   if (g == 128) return fmt == MOE_SCALE_UE8M0_U8 || fmt == MOE_SCALE_UE8M0_PACKED ||
-                       fmt == MOE_SCALE_F32_POW2;
-  if (g == 32) return fmt == MOE_SCALE_UE8M0_U8;
+                       fmt == MOE_SCALE_F32_POW2 || fmt == MOE_SCALE_F32;
+  if (g == 32) return fmt == MOE_SCALE_UE8M0_U8 || fmt == MOE_SCALE_MX_E8M0;
   return false;
 }
 
@@ -122,8 +122,8 @@ int32_t moe_should_use_masked(int32_t E, int32_t L) { return (E > L && L <= 32) 
 size_t moe_scale_bytes(moe_scale_fmt_t fmt, int64_t rows, int32_t H, int32_t g) {
   if (rows < 0 || H <= 0 || (g != 32 && g != 128) || H % g || !fmt_ok(fmt, g)) return 0;
   const int64_t G = H / g;
-  if (fmt == MOE_SCALE_UE8M0_U8) return (size_t)(rows * G);
-  if (fmt == MOE_SCALE_F32_POW2) return (size_t)(rows * G * 4);
+  if (fmt == MOE_SCALE_UE8M0_U8 || fmt == MOE_SCALE_MX_E8M0) return (size_t)(rows * G);
+  if (fmt == MOE_SCALE_F32_POW2 || fmt == MOE_SCALE_F32) return (size_t)(rows * G * 4);
   return (size_t)(((G + 3) / 4) * 4 * ((rows + 3) / 4 * 4));
 }
 
@@ -268,20 +268,43 @@ moe_status_t moe_expand_from_slab(const void* slab, int32_t elem_bytes, int32_t 
                        reinterpret_cast<cudaStream_t>(stream));
 }
 
-moe_status_t fp8_requant_per_tensor(const void* q, int64_t ldq, const float* s_tok, int32_t T,
-                                    int32_t H, void* q_out, float* d_scale_out,
-                                    moe_stream_t stream) {
+static moe_status_t requant_common(const void* q, int64_t ldq, const void* s_tok, int s_fmt,
+                                   int32_t T, int32_t H, int mode, void* q_out, float* d_scale_out,
+                                   void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   if (T < 0 || H <= 0 || H % 16 || !d_scale_out) return MOE_ERR_INVALID_ARG;
+  if (s_fmt != MOE_TOKSCALE_F32 && s_fmt != MOE_TOKSCALE_UE8M0) return MOE_ERR_INVALID_ARG;
+  if (mode != MOE_REQUANT_MAX_SCALE && mode != MOE_REQUANT_AMAX) return MOE_ERR_INVALID_ARG;
   if (T > 0) {
     if (!q || !aligned16(q) || ldq < H || ldq % 16 || !s_tok) return MOE_ERR_INVALID_ARG;
     if (!q_out || !aligned16(q_out)) return MOE_ERR_INVALID_ARG;
+    if (mode == MOE_REQUANT_AMAX &&
+        (!workspace || !aligned16(workspace) || workspace_bytes < (size_t)T * sizeof(float)))
+      return MOE_ERR_INVALID_ARG;
   }
   const int sms = num_sms_cached();
   if (sms <= 0) return MOE_ERR_CUDA;
   RequantArgs ra{};
-  ra.q = static_cast<const uint8_t*>(q); ra.ldq = ldq; ra.s_tok = s_tok; ra.T = T; ra.H = H;
+  ra.q = static_cast<const uint8_t*>(q); ra.ldq = ldq; ra.s_tok = s_tok;
+  ra.s_fmt = s_fmt; ra.mode = mode; ra.T = T; ra.H = H;
   ra.q_out = static_cast<uint8_t*>(q_out); ra.scale_out = d_scale_out;
-  return cuda_status(launch_requant(ra, sms, reinterpret_cast<cudaStream_t>(stream)));
+  ra.ws = static_cast<float*>(workspace);
+  return cuda_status(launch_requant(ra, sms, stream));
+}
+
+moe_status_t fp8_requant_per_tensor(const void* q, int64_t ldq, const float* s_tok, int32_t T,
+                                    int32_t H, void* q_out, float* d_scale_out,
+                                    moe_stream_t stream) {
+  return requant_common(q, ldq, s_tok, MOE_TOKSCALE_F32, T, H, MOE_REQUANT_MAX_SCALE, q_out,
+                        d_scale_out, nullptr, 0, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t fp8_requant_per_tensor_ex(const void* q, int64_t ldq, const void* s_tok,
+                                       moe_tokscale_fmt_t s_fmt, int32_t T, int32_t H,
+                                       moe_requant_mode_t mode, void* q_out, float* d_scale_out,
+                                       void* workspace, size_t workspace_bytes,
+                                       moe_stream_t stream) {
+  return requant_common(q, ldq, s_tok, (int)s_fmt, T, H, (int)mode, q_out, d_scale_out,
+                        workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 moe_status_t moe_status_sync(const int32_t* d_status, moe_stream_t stream) {

@@ -23,7 +23,9 @@ constexpr int kStBadLayout = 0x4;
 // Scale layouts (same values as moe_scale_fmt_t).
 constexpr int kFmtU8 = 0;
 constexpr int kFmtPacked = 1;
-constexpr int kFmtF32 = 2;
+constexpr int kFmtF32Pow2 = 2;
+constexpr int kFmtF32 = 3;   // plain fp32 group scale amax / 448
+constexpr int kFmtMX = 4;    // OCP MX E8M0 (floor exponent, saturating elements)
 
 // Route-plan modes.
 constexpr int kModeCompact = 0;
@@ -102,9 +104,28 @@ __device__ __forceinline__ int group_exponent(float amax) {
   return min(max(e, -127), 127);
 }
 
-// 2^-e as a float (e in [-126, 126]).
+// OCP MX shared exponent for E4M3 elements: floor(log2(amax)) - 8, at least
+// -127 (zero and tiny amax give -127). For a normal float the floor of log2 is
+// its unbiased exponent field.
+__device__ __forceinline__ int mx_exponent(float amax) {
+  const int Eb = (int)(__float_as_uint(amax) >> 23) & 0xFF;
+  return max(Eb - 135, -127);
+}
+
+// 2^-e as a float (e in [-127, 126]).
 __device__ __forceinline__ float exp2_neg(int e) {
-  return __uint_as_float((uint32_t)(127 - e) << 23);
+  return __uint_as_float((uint32_t)(127 - e) << 23);  // e = -127 gives 2^127
+}
+
+// Quantise 8 bf16 values by an fp32 scale s: RNE_e4m3(fl32(x / s)), one IEEE
+// fp32 division per element.
+__device__ __forceinline__ uint2 quant8_div(const uint4& v, float s) {
+  uint2 r;
+  r.x = cvt_e4m3x2(__fdiv_rn(bf16_lo(v.x), s), __fdiv_rn(bf16_hi(v.x), s)) |
+        (cvt_e4m3x2(__fdiv_rn(bf16_lo(v.y), s), __fdiv_rn(bf16_hi(v.y), s)) << 16);
+  r.y = cvt_e4m3x2(__fdiv_rn(bf16_lo(v.z), s), __fdiv_rn(bf16_hi(v.z), s)) |
+        (cvt_e4m3x2(__fdiv_rn(bf16_lo(v.w), s), __fdiv_rn(bf16_hi(v.w), s)) << 16);
+  return r;
 }
 
 // Quantise 8 bf16 values (one 16-byte vector) by 2^-e into 8 e4m3 bytes.
@@ -143,6 +164,30 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 }
 __device__ __forceinline__ void pdl_wait_primary() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Bulk (TMA) copy of `bytes` from shared memory to global memory, tracked in
+// the issuing thread's bulk groups. Both addresses 16-byte aligned, bytes a
+// multiple of 16.
+__device__ __forceinline__ void bulk_store_s2g(void* gdst, uint32_t ssrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+               ::"l"(gdst), "r"(ssrc), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Wait until at most N of this thread's bulk groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+// Make this thread's generic-proxy shared-memory writes visible to bulk copies.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ int64_t align_up64(int64_t c, int64_t b) { return (c + b - 1) / b * b; }

@@ -103,13 +103,19 @@ cudaError_t launch_repack(const RepackArgs& a, int num_sms, cudaStream_t s);
 // ---------------------------------------------------------------------------
 // Per-token -> per-tensor requant
 // ---------------------------------------------------------------------------
+constexpr int kTokScaleF32 = 0;    // per-token scales: fp32
+constexpr int kTokScaleE8M0 = 1;   // per-token scales: e8m0 bytes, 2^(b - 127)
+constexpr int kRequantMaxScale = 0;
+constexpr int kRequantAmax = 1;
 struct RequantArgs {
   const uint8_t* q;
   int64_t ldq;
-  const float* s_tok;
+  const void* s_tok;
+  int32_t s_fmt, mode;
   int32_t T, H;
   uint8_t* q_out;
   float* scale_out;
+  float* ws;                   // amax mode: [T] per-row s * amax
 };
 cudaError_t launch_requant(const RequantArgs& a, int num_sms, cudaStream_t s);
 

@@ -20,20 +20,23 @@
 //
 // Design: a persistent grid (SMs x resident CTAs, independent of the routing)
 // walks the live tokens, t = blockIdx.x + i * gridDim.x. One thread owns two
-// 16-element chunks of a row (two 16-byte loads each, one 16-byte e4m3 store
-// per destination), so a single pass covers H <= 32768.
+// 16-element chunks of a row (two 16-byte loads each), so a single pass
+// covers H <= 32768.
 //   Prologue: the CTA issues its first token's loads, then waits for the route
 //   plan (programmatic dependent launch: this grid is already resident while
 //   the route plan runs), loads the chunk table (<= 64 KiB) into shared memory,
 //   scans it, and resolves the rows of all of its own slots at once. The
-//   route plan therefore needs no serial "last block" and no fence, and the
-//   token loop never waits at a barrier.
-//   Token loop: the next token's loads are issued before the current token's
-//   stores; the g/16 lanes of a group reduce the group max with xor shuffles on
-//   sign-cleared bf16 bit patterns; the exponent comes from the float's bit
-//   fields; conversion is cvt.rn.satfinite.e4m3x2.f32. A warp writes 512
-//   contiguous bytes per destination row, and for the packed UE8M0 layout
-//   exactly one 32-bit scale word (4 groups of 128).
+//   route plan therefore needs no serial "last block" and no fence.
+//   Token loop: the next token's loads are issued before the current token is
+//   processed; the g/16 lanes of a group reduce the group max with xor
+//   shuffles on sign-cleared bf16 bit patterns; the exponent comes from the
+//   float's bit fields; conversion is cvt.rn.satfinite.e4m3x2.f32. The e4m3
+//   row is staged in shared memory and thread 0 writes it to each of the
+//   token's destination rows with one bulk (TMA) copy per row, so the payload
+//   -- 80% of the kernel's traffic -- leaves the SM as large asynchronous
+//   transfers instead of per-thread stores. Scales are small direct stores:
+//   for the packed UE8M0 layout exactly one 32-bit word per warp (4 groups of
+//   128) per destination.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -41,12 +44,34 @@ namespace moeperm {
 
 namespace {
 
-constexpr int kCPT = 2;  // 16-element chunks per thread
+#ifndef MOEPERM_SCATTER_STAGES
+#define MOEPERM_SCATTER_STAGES 3
+#endif
+#ifndef MOEPERM_SCATTER_CPT
+#define MOEPERM_SCATTER_CPT 2
+#endif
+constexpr int kCPT = MOEPERM_SCATTER_CPT;          // 16-element chunks per thread
+constexpr int kStages = MOEPERM_SCATTER_STAGES;    // staged rows in flight to the bulk-copy engine
+
+// Dynamic shared memory: [table nchunks*L | starts L | psum L | rows ntok*K]
+// (dispatch modes only), then kStages staged rows of H bytes at a 128-byte
+// boundary.
+__host__ __device__ inline size_t layout_bytes(const ScatterArgs& p, int64_t ntok) {
+  if (p.mode == kModeIdentity) return 0;
+  return ((size_t)p.nchunks * p.L + 2 * (size_t)p.L + (size_t)ntok * p.K) * sizeof(int32_t);
+}
+__host__ __device__ inline size_t stage_offset(const ScatterArgs& p, int64_t ntok) {
+  return (layout_bytes(p, ntok) + 127) / 128 * 128;
+}
+// Tokens per CTA the row buffer is sized for (ceil(T / grid)).
+__device__ inline int64_t ntok_smem(const ScatterArgs& p) {
+  return ((int64_t)p.T + gridDim.x - 1) / gridDim.x;
+}
 
 template <int GSZ, int FMT>
 __device__ __forceinline__ void store_scales(const ScatterArgs& p, int nslots, const int* rows,
-                                             int lane, bool active, int e, int group_base,
-                                             int G, int G4) {
+                                             int lane, bool active, int e, float sval,
+                                             int group_base, int G, int G4) {
   constexpr int GL = GSZ / 16;  // lanes per group
   constexpr int GPW = 32 / GL;  // groups per warp
   const uint32_t byte = active ? (uint32_t)(e + 127) : 0u;
@@ -72,7 +97,7 @@ __device__ __forceinline__ void store_scales(const ScatterArgs& p, int nslots, c
         sc[pk + wofs] = word;
       }
     }
-  } else if constexpr (FMT == kFmtU8) {
+  } else if constexpr (FMT == kFmtU8 || FMT == kFmtMX) {
     constexpr int WPW = GPW / 4;  // whole 4-group words per warp
     const int q = lane % WPW;
     uint32_t word = 0;
@@ -90,10 +115,10 @@ __device__ __forceinline__ void store_scales(const ScatterArgs& p, int nslots, c
       for (int k = 0; k < nslots; ++k)
         if (rows[k] >= 0) sc[(int64_t)rows[k] * p.ld_s + gidx] = (uint8_t)byte;
     }
-  } else {
+  } else {  // fp32 scales: 2^e, or the plain amax / 448
     if (leader) {
       float* sc = reinterpret_cast<float*>(p.scales);
-      const float v = __uint_as_float((uint32_t)(e + 127) << 23);
+      const float v = (FMT == kFmtF32) ? sval : __uint_as_float((uint32_t)(e + 127) << 23);
       for (int k = 0; k < nslots; ++k)
         if (rows[k] >= 0) sc[(int64_t)rows[k] * p.ld_s + gidx] = v;
     }
@@ -251,7 +276,15 @@ __global__ void __launch_bounds__(1024) quant_scatter_kernel(ScatterArgs p) {
     __syncthreads();
   }
 
-  // ---- token loop: no barriers ---------------------------------------------
+  // ---- token loop ---------------------------------------------------------
+  // The quantised row is staged in shared memory (kStages rotating buffers)
+  // and thread 0 writes it to every destination row with bulk copies, so the
+  // payload stores leave the SM as a few large TMA transfers. One barrier per
+  // token publishes the staged row; before it, thread 0 waits until the bulk
+  // copies that last read the NEXT buffer are done, so after it every thread
+  // may overwrite that buffer.
+  uint8_t* stage = reinterpret_cast<uint8_t*>(sm) + stage_offset(p, ntok_smem(p));
+  const uint32_t stage_s = (uint32_t)__cvta_generic_to_shared(stage);
   int ident_row[1];
   for (int it = 0; it < ntok; ++it) {
     const int t = blockIdx.x + it * gridDim.x;
@@ -265,6 +298,8 @@ __global__ void __launch_bounds__(1024) quant_scatter_kernel(ScatterArgs p) {
     } else {
       rows = rows_s + it * p.K;
     }
+    const int buf = it % kStages;
+    uint8_t* sb = stage + (size_t)buf * H;
 #pragma unroll
     for (int i = 0; i < kCPT; ++i) {
       const int c = i * bd + tid;
@@ -272,19 +307,34 @@ __global__ void __launch_bounds__(1024) quant_scatter_kernel(ScatterArgs p) {
       uint32_t m = amax16_bf16(v[i][0], v[i][1]);
 #pragma unroll
       for (int off = 1; off < GSZ / 16; off <<= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
-      const int e = group_exponent(__uint_as_float(m << 16));
-      const float inv = exp2_neg(e);
-      const uint2 q0 = quant8(v[i][0], inv), q1 = quant8(v[i][1], inv);
-      const uint4 q = make_uint4(q0.x, q0.y, q1.x, q1.y);
-      if (active) {
-        for (int k = 0; k < nslots; ++k) {
-          const int row = rows[k];
-          if (row >= 0) st_v4(p.xq + (int64_t)row * H + c * 16, q);
-        }
+      const float amax = __uint_as_float(m << 16);
+      int e = 0;
+      float sval = 0.0f;
+      uint2 q0, q1;
+      if constexpr (FMT == kFmtF32) {
+        sval = __fdiv_rn(fmaxf(amax, 1e-10f), 448.0f);
+        q0 = quant8_div(v[i][0], sval);
+        q1 = quant8_div(v[i][1], sval);
+      } else {
+        e = (FMT == kFmtMX) ? mx_exponent(amax) : group_exponent(amax);
+        const float inv = exp2_neg(e);
+        q0 = quant8(v[i][0], inv);
+        q1 = quant8(v[i][1], inv);
       }
+      if (active) *reinterpret_cast<uint4*>(sb + c * 16) = make_uint4(q0.x, q0.y, q1.x, q1.y);
       const int cw = i * bd + (tid & ~31);  // first chunk of this warp
       if (cw < nch)
-        store_scales<GSZ, FMT>(p, nslots, rows, lane, active, e, cw * 16 / GSZ, G, G4);
+        store_scales<GSZ, FMT>(p, nslots, rows, lane, active, e, sval, cw * 16 / GSZ, G, G4);
+    }
+    fence_proxy_async_smem();
+    if (tid == 0) bulk_wait_read<kStages - 2>();
+    __syncthreads();
+    if (tid == 0) {
+      for (int k = 0; k < nslots; ++k) {
+        const int row = rows[k];
+        if (row >= 0) bulk_store_s2g(p.xq + (int64_t)row * H, stage_s + (uint32_t)(buf * H), (uint32_t)H);
+      }
+      bulk_commit();
     }
 #pragma unroll
     for (int i = 0; i < kCPT; ++i) {
@@ -292,6 +342,7 @@ __global__ void __launch_bounds__(1024) quant_scatter_kernel(ScatterArgs p) {
       v[i][1] = vn[i][1];
     }
   }
+  if (tid == 0) bulk_wait_all();
 }
 
 template <int GSZ, int FMT>
@@ -300,23 +351,19 @@ cudaError_t launch_one(const ScatterArgs& a, int num_sms, bool pdl, cudaStream_t
   int bd = (nch + kCPT - 1) / kCPT;
   bd = (bd + 31) / 32 * 32;
   if (bd > 1024) return cudaErrorInvalidValue;  // H > 32768 is rejected on the host
-  size_t fixed = 0, per_token = 0;
-  if (a.mode != kModeIdentity) {
-    fixed = ((size_t)a.nchunks * a.L + 2 * (size_t)a.L) * sizeof(int32_t);
-    per_token = (size_t)a.K * sizeof(int32_t);
-  }
-  // Resident CTAs per SM with a provisional row buffer of 8 tokens per CTA;
+  // Resident CTAs per SM with a provisional row buffer of 16 tokens per CTA;
   // the grid is then fixed and the row buffer sized for ceil(T / grid) tokens.
   int per_sm = 0;
   cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      &per_sm, quant_scatter_kernel<GSZ, FMT>, bd, fixed + 8 * per_token);
+      &per_sm, quant_scatter_kernel<GSZ, FMT>, bd,
+      stage_offset(a, 16) + (size_t)kStages * a.H);
   if (err != cudaSuccess) return err;
   if (per_sm < 1) per_sm = 1;
   int64_t grid = (int64_t)num_sms * per_sm;
   if (grid > a.T) grid = a.T;
   if (grid < 1) grid = 1;
   const int64_t ntok_max = (a.T + grid - 1) / grid;
-  const size_t smem = fixed + (size_t)ntok_max * per_token;
+  const size_t smem = stage_offset(a, ntok_max) + (size_t)kStages * a.H;
   if (smem > 48 * 1024) {
     err = cudaFuncSetAttribute(quant_scatter_kernel<GSZ, FMT>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -342,8 +389,10 @@ cudaError_t launch_quant_scatter(const ScatterArgs& a, int g, int fmt, int num_s
   if (g == 128) {
     if (fmt == kFmtPacked) return launch_one<128, kFmtPacked>(a, num_sms, after_route_plan, s);
     if (fmt == kFmtU8) return launch_one<128, kFmtU8>(a, num_sms, after_route_plan, s);
-    return launch_one<128, kFmtF32>(a, num_sms, after_route_plan, s);
+    if (fmt == kFmtF32) return launch_one<128, kFmtF32>(a, num_sms, after_route_plan, s);
+    return launch_one<128, kFmtF32Pow2>(a, num_sms, after_route_plan, s);
   }
+  if (fmt == kFmtMX) return launch_one<32, kFmtMX>(a, num_sms, after_route_plan, s);
   return launch_one<32, kFmtU8>(a, num_sms, after_route_plan, s);
 }
 

@@ -104,7 +104,7 @@ __global__ void __launch_bounds__(kThreads) repack_kernel(RepackArgs p) {
           if (w == G4 - 1 && (G & 3)) word &= (1u << (8 * (G & 3))) - 1u;
           d32[p.to_slab ? sw : xw] = word;
         }
-      } else if (p.fmt == kFmtU8) {
+      } else if (p.fmt == kFmtU8 || p.fmt == kFmtMX) {
         const uint8_t* s8 = reinterpret_cast<const uint8_t*>(p.src_scales);
         uint8_t* d8 = reinterpret_cast<uint8_t*>(p.dst_scales);
         const int64_t so = (p.to_slab ? r : srow) * p.ld_src_s;

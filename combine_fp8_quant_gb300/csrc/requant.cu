@@ -1,16 +1,25 @@
 // requant.cu -- per-token -> per-tensor FP8 requantisation
-// (PR #14162 实现拆解 items 1-2, fp8_per_token_to_per_tensor_quant; the
-// per-token scales are plain fp32, 风险与影响 item 3).
+// (PR #14162 实现拆解 items 1-2, fp8_per_token_to_per_tensor_quant; 风险与影响
+// item 3: the original kernel assumes plain fp32 per-token scales and does not
+// handle e8m0 ones).
 //
-//   S = max_t s[t]  (S = 1 if T = 0 or all scales are 0)
-//   q_out[t, h] = RNE_e4m3( fp32( decode(q[t, h]) * fp32(s[t] / S) ) )
+//   s[t]  = the token's scale: fp32, or 2^(b - 127) for an e8m0 byte b
+//   S     = max_t s[t]                                   (max-scale mode)
+//         = fl32(max_t fl32(s[t] * amax_t) / 448)        (amax mode, amax_t =
+//           max_h |decode(q[t,h])|: the largest dequantised value maps to 448)
+//   S = 1 if T = 0 or the maximum is 0 (then r = 0)
+//   q_out[t, h] = RNE_e4m3( fl32( decode(q[t, h]) * fl32(s[t] / S) ) )
 //
-// Design: one launch. Every CTA first reduces the T scales itself (they are a
-// few KB and L2-resident, so the redundant reads cost less than a second
-// launch), then streams whole rows: 16 e4m3 bytes per thread per step, widened
-// exactly with cvt.rn.f16x2.e4m3x2, scaled in fp32, narrowed with
-// cvt.rn.satfinite.e4m3x2.f32. The sources hard-code a 1024-wide hidden block;
-// here the row is covered by the whole CTA with 16-byte vectors instead.
+// Design: the max-scale mode is one launch. Every CTA first issues its first
+// row's loads, then reduces the T scales itself (float4 / byte loads, L2-
+// resident) while they are in flight, and streams rows: 16 e4m3 bytes per
+// thread per step, widened exactly with cvt.rn.f16x2.e4m3x2, scaled in fp32,
+// narrowed with cvt.rn.satfinite.e4m3x2.f32. The amax mode adds a first launch
+// that writes fl32(s[t] * amax_t) per row to the workspace (the row maximum is
+// a byte-wise __vmaxu4 of sign-cleared codes: for finite e4m3 the code order is
+// the magnitude order); the second launch reduces that array instead of the
+// scales. q (tens of MB) is still in L2 for the second read. The sources
+// hard-code a 1024-wide hidden block; here a CTA covers the whole row.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -27,31 +36,83 @@ __device__ __forceinline__ uint32_t requant4(uint32_t w, float r) {
          (cvt_e4m3x2(__fmul_rn(b.x, r), __fmul_rn(b.y, r)) << 16);
 }
 
-__device__ __forceinline__ float block_max_scales(const RequantArgs& p, float* s_red) {
+// 2^(b - 127) for an e8m0 byte (b = 0 is the fp32 subnormal 2^-127).
+__device__ __forceinline__ float e8m0_value(uint32_t b) {
+  return b == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(b << 23);
+}
+
+template <int SFMT>
+__device__ __forceinline__ float token_scale(const RequantArgs& p, int t) {
+  if constexpr (SFMT == kTokScaleF32) return __ldg(reinterpret_cast<const float*>(p.s_tok) + t);
+  else return e8m0_value(__ldg(reinterpret_cast<const uint8_t*>(p.s_tok) + t));
+}
+
+__device__ __forceinline__ float block_max(float m, float* s_red) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  float m = 0.0f;
-  const int T4 = p.T / 4;
-  const bool vec = (reinterpret_cast<uintptr_t>(p.s_tok) & 15u) == 0;
-  if (vec) {
-    const float4* s4 = reinterpret_cast<const float4*>(p.s_tok);
-    for (int i = tid; i < T4; i += kThreads) {
-      const float4 v = __ldg(s4 + i);
-      m = fmaxf(fmaxf(m, fmaxf(v.x, v.y)), fmaxf(v.z, v.w));
-    }
-    for (int t = 4 * T4 + tid; t < p.T; t += kThreads) m = fmaxf(m, __ldg(p.s_tok + t));
-  } else {
-    for (int t = tid; t < p.T; t += kThreads) m = fmaxf(m, __ldg(p.s_tok + t));
-  }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
   if (lane == 0) s_red[warp] = m;
   __syncthreads();
-  float S = 0.0f;
+  float r = 0.0f;
 #pragma unroll
-  for (int w = 0; w < kThreads / 32; ++w) S = fmaxf(S, s_red[w]);
-  return S;
+  for (int w = 0; w < kThreads / 32; ++w) r = fmaxf(r, s_red[w]);
+  return r;
 }
 
+// max over n non-negative floats (float4 loads when aligned)
+__device__ __forceinline__ float reduce_floats(const float* a, int n, float* s_red) {
+  const int tid = threadIdx.x;
+  float m = 0.0f;
+  if ((reinterpret_cast<uintptr_t>(a) & 15u) == 0) {
+    const float4* a4 = reinterpret_cast<const float4*>(a);
+    for (int i = tid; i < n / 4; i += kThreads) {
+      const float4 v = __ldcg(a4 + i);
+      m = fmaxf(fmaxf(m, fmaxf(v.x, v.y)), fmaxf(v.z, v.w));
+    }
+    for (int t = 4 * (n / 4) + tid; t < n; t += kThreads) m = fmaxf(m, __ldcg(a + t));
+  } else {
+    for (int t = tid; t < n; t += kThreads) m = fmaxf(m, __ldcg(a + t));
+  }
+  return block_max(m, s_red);
+}
+
+// max over n e8m0 bytes, as the scale value
+__device__ __forceinline__ float reduce_e8m0(const uint8_t* b, int n, float* s_red) {
+  uint32_t m = 0;
+  for (int t = threadIdx.x; t < n; t += kThreads) m = max(m, (uint32_t)__ldg(b + t));
+  return block_max(m ? e8m0_value(m) : 0.0f, s_red);
+}
+
+// amax mode, launch 1: ws[t] = fl32(s[t] * max_h |decode(q[t, h])|)
+template <int SFMT>
+__global__ void __launch_bounds__(kThreads) requant_rowmax_kernel(RequantArgs p) {
+  __shared__ uint32_t s_red[kThreads / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nch = p.H / 16;
+  for (int t = blockIdx.x; t < p.T; t += gridDim.x) {
+    const uint8_t* src = p.q + (int64_t)t * p.ldq;
+    uint32_t m = 0;
+    for (int c = tid; c < nch; c += kThreads) {
+      const uint4 v = ld_nc_v4(src + (int64_t)c * 16);
+      const uint32_t k = 0x7F7F7F7Fu;
+      m = __vmaxu4(m, __vmaxu4(__vmaxu4(v.x & k, v.y & k), __vmaxu4(v.z & k, v.w & k)));
+    }
+    m = max(max(m & 0xFFu, (m >> 8) & 0xFFu), max((m >> 16) & 0xFFu, m >> 24));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
+    if (lane == 0) s_red[warp] = m;
+    __syncthreads();
+    if (tid == 0) {
+      uint32_t mm = 0;
+      for (int w = 0; w < kThreads / 32; ++w) mm = max(mm, s_red[w]);
+      const float amax = e4m3x2_to_float2(mm).x;
+      p.ws[t] = __fmul_rn(token_scale<SFMT>(p, t), amax);
+    }
+    __syncthreads();
+  }
+}
+
+template <int SFMT, int MODE>
 __global__ void __launch_bounds__(kThreads) requant_kernel(RequantArgs p) {
   __shared__ float s_red[kThreads / 32];
   const int tid = threadIdx.x;
@@ -66,11 +127,18 @@ __global__ void __launch_bounds__(kThreads) requant_kernel(RequantArgs p) {
     if (tid < nch) a = ld_nc_v4(src + (int64_t)tid * 16);
     if (tid + kThreads < nch) b = ld_nc_v4(src + (int64_t)(tid + kThreads) * 16);
   }
-  const float S = block_max_scales(p, s_red);
+  float S;
+  if constexpr (MODE == kRequantAmax) {
+    S = __fdiv_rn(reduce_floats(p.ws, p.T, s_red), 448.0f);
+  } else if constexpr (SFMT == kTokScaleF32) {
+    S = reduce_floats(reinterpret_cast<const float*>(p.s_tok), p.T, s_red);
+  } else {
+    S = reduce_e8m0(reinterpret_cast<const uint8_t*>(p.s_tok), p.T, s_red);
+  }
   if (blockIdx.x == 0 && tid == 0) *p.scale_out = (S > 0.0f) ? S : 1.0f;
 
   for (; t < p.T; t += gridDim.x) {
-    const float r = (S > 0.0f) ? __fdiv_rn(__ldg(p.s_tok + t), S) : 0.0f;
+    const float r = (S > 0.0f) ? __fdiv_rn(token_scale<SFMT>(p, t), S) : 0.0f;
     const uint8_t* src = p.q + (int64_t)t * p.ldq;
     uint8_t* dst = p.q_out + (int64_t)t * p.H;
     for (int c = tid; c < nch; c += 2 * kThreads) {
@@ -96,18 +164,34 @@ __global__ void __launch_bounds__(kThreads) requant_kernel(RequantArgs p) {
   }
 }
 
-}  // namespace
-
-cudaError_t launch_requant(const RequantArgs& a, int num_sms, cudaStream_t s) {
+template <typename Kern>
+cudaError_t launch_rows(Kern k, const RequantArgs& a, int num_sms, cudaStream_t s) {
   int per_sm = 0;
-  cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, requant_kernel, kThreads, 0);
+  cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kThreads, 0);
   if (err != cudaSuccess) return err;
   if (per_sm < 1) per_sm = 1;
   int64_t grid = (int64_t)num_sms * per_sm;
   if (grid > a.T) grid = a.T;
   if (grid < 1) grid = 1;
-  requant_kernel<<<(unsigned)grid, kThreads, 0, s>>>(a);
+  k<<<(unsigned)grid, kThreads, 0, s>>>(a);
   return cudaGetLastError();
+}
+
+template <int SFMT>
+cudaError_t launch_fmt(const RequantArgs& a, int num_sms, cudaStream_t s) {
+  if (a.mode == kRequantAmax) {
+    cudaError_t err = launch_rows(requant_rowmax_kernel<SFMT>, a, num_sms, s);
+    if (err != cudaSuccess) return err;
+    return launch_rows(requant_kernel<SFMT, kRequantAmax>, a, num_sms, s);
+  }
+  return launch_rows(requant_kernel<SFMT, kRequantMaxScale>, a, num_sms, s);
+}
+
+}  // namespace
+
+cudaError_t launch_requant(const RequantArgs& a, int num_sms, cudaStream_t s) {
+  return a.s_fmt == kTokScaleF32 ? launch_fmt<kTokScaleF32>(a, num_sms, s)
+                                 : launch_fmt<kTokScaleE8M0>(a, num_sms, s);
 }
 
 }  // namespace moeperm

@@ -29,6 +29,9 @@ namespace {
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kGroup = 8;  // steps whose peer masks are formed together
+#ifndef MOEPERM_ROUTE_MAX_CHUNKS
+#define MOEPERM_ROUTE_MAX_CHUNKS 16
+#endif
 
 template <int S>
 __global__ void __launch_bounds__(kThreads) route_plan_kernel(RoutePlanArgs p) {
@@ -120,7 +123,7 @@ int route_plan_S(int64_t A, int L) {
   const int cand[] = {1, 4, 16, 64};
   for (int S : cand) {
     const int64_t nc = (A + (int64_t)kThreads * S - 1) / ((int64_t)kThreads * S);
-    if (nc <= 16 && nc * L <= kMaxTableInts) return S;
+    if (nc <= MOEPERM_ROUTE_MAX_CHUNKS && nc * L <= kMaxTableInts) return S;
   }
   for (int S : cand) {
     const int64_t nc = (A + (int64_t)kThreads * S - 1) / ((int64_t)kThreads * S);

@@ -26,7 +26,7 @@ LIB_PATH = os.path.join(HERE, "libmoeperm.so")
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_OVERFLOW = 0, 1, 2
 MOE_ERR_LIVE_OVERFLOW, MOE_ERR_BAD_LAYOUT, MOE_ERR_CUDA = 3, 4, 5
 STATUS_OVERFLOW, STATUS_LIVE_OVERFLOW, STATUS_BAD_LAYOUT = 1, 2, 4
-FMT = {"u8": 0, "packed": 1, "f32": 2}
+FMT = {"u8": 0, "packed": 1, "f32pow2": 2, "f32": 3, "mx": 4}
 
 _lock = threading.Lock()
 _lib = None
@@ -77,6 +77,7 @@ def _declare(L):
         "moe_expand_from_slab": (i32, [vp, i32, i32, vp, i64, vp, i32, i32, i32, i32, i32, vp, vp,
                                        i64, vp, i64, vp, vp, vp]),
         "fp8_requant_per_tensor": (i32, [vp, i64, vp, i32, i32, vp, vp, vp]),
+        "fp8_requant_per_tensor_ex": (i32, [vp, i64, vp, i32, i32, i32, i32, vp, vp, vp, sz, vp]),
         "moe_status_sync": (i32, [vp, vp]),
         "moe_status_string": (C.c_char_p, [i32]),
         "moe_version": (C.c_char_p, []),
@@ -196,6 +197,17 @@ def fp8_requant_per_tensor(q, ldq, s_tok, T, H, q_out, d_scale_out, stream=None)
                                             _ptr(d_scale_out), _stream(stream)))
 
 
+TOKSCALE = {"f32": 0, "ue8m0": 1}
+REQUANT_MODE = {"max_scale": 0, "amax": 1}
+
+
+def fp8_requant_per_tensor_ex(q, ldq, s_tok, s_fmt, T, H, mode, q_out, d_scale_out, workspace,
+                              workspace_bytes, stream=None) -> int:
+    return int(lib().fp8_requant_per_tensor_ex(
+        _ptr(q), ldq, _ptr(s_tok), TOKSCALE[s_fmt], T, H, REQUANT_MODE[mode], _ptr(q_out),
+        _ptr(d_scale_out), _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
 def moe_status_sync(d_status, stream=None) -> int:
     return int(lib().moe_status_sync(_ptr(d_status), _stream(stream)))
 
@@ -209,14 +221,14 @@ def moe_version() -> str:
 # ---------------------------------------------------------------------------
 
 def scale_tensor(fmt: str, rows: int, H: int, g: int, device, blocks: int = 1, ld: int | None = None):
-    """Allocate a scale tensor in `fmt`: u8 -> uint8 [rows, G]; f32 -> float32
+    """Allocate a scale tensor in `fmt`: u8 -> uint8 [rows, G]; f32pow2 -> float32
     [rows, G]; packed -> int32 [blocks, G4, ld] (ld = rows per block rounded up
     to 4). Returns (tensor, ld)."""
     G = H // g
-    if fmt == "u8":
+    if fmt in ("u8", "mx"):
         ld = G if ld is None else ld
         return torch.empty((rows, ld), dtype=torch.uint8, device=device), ld
-    if fmt == "f32":
+    if fmt in ("f32pow2", "f32"):
         ld = G if ld is None else ld
         return torch.empty((rows, ld), dtype=torch.float32, device=device), ld
     rpb = rows // blocks

@@ -89,14 +89,24 @@ typedef enum {
  *                         columns). Word w holds groups 4w..4w+3, group 4w in the
  *                         least significant byte; bytes past group G-1 are 0.
  *  MOE_SCALE_F32_POW2     float [rows, ld_s], ld_s >= G; element (r, j) = 2^e.
+ *  MOE_SCALE_F32          float [rows, ld_s], ld_s >= G; a plain fp32 group scale
+ *                         s = fl32(max(amax, 1e-10) / 448) and q = RNE_e4m3(fl32(x / s))
+ *                         (the fp32-scale form that direct UE8M0 replaces
+ *                         [P1 实现拆解 item 3]; [P4 功能与动机: group-128 fp32 scales]).
+ *  MOE_SCALE_MX_E8M0      uint8 [rows, ld_s] like MOE_SCALE_UE8M0_U8, but with the
+ *                         OCP MX exponent rule: X = floor(log2 amax) - 8 (at least
+ *                         -127), byte X + 127, q = RNE_e4m3(x * 2^-X) saturated to
+ *                         +-448 (the block maximum lands in [256, 512)).
  *
- * Supported (format, group) pairs: g = 128 with any of the three; g = 32 with
- * MOE_SCALE_UE8M0_U8 (the MXFP8 layout).
+ * Supported (format, group) pairs: g = 128 with U8, PACKED, F32_POW2 or F32;
+ * g = 32 with U8 (the MXFP8 layout of [P4]) or MX_E8M0.
  */
 typedef enum {
   MOE_SCALE_UE8M0_U8 = 0,
   MOE_SCALE_UE8M0_PACKED = 1,
-  MOE_SCALE_F32_POW2 = 2
+  MOE_SCALE_F32_POW2 = 2,
+  MOE_SCALE_F32 = 3,
+  MOE_SCALE_MX_E8M0 = 4
 } moe_scale_fmt_t;
 
 /* ------------------------------------------------------------------ */
@@ -333,6 +343,33 @@ moe_status_t moe_expand_from_slab(
 moe_status_t fp8_requant_per_tensor(
     const void* q, int64_t ldq, const float* s_tok, int32_t T, int32_t H, void* q_out,
     float* d_scale_out, moe_stream_t stream);
+
+/* Per-token input scale format and per-tensor scale rule of the extended requant. */
+typedef enum {
+  MOE_TOKSCALE_F32 = 0,    /* float [T] */
+  MOE_TOKSCALE_UE8M0 = 1   /* uint8 [T] e8m0 bytes: scale 2^(b - 127) (b = 255 is out of contract) */
+} moe_tokscale_fmt_t;
+typedef enum {
+  MOE_REQUANT_MAX_SCALE = 0, /* S = max_t s[t] */
+  MOE_REQUANT_AMAX = 1       /* S = fl32(max_t fl32(s[t] * amax_t) / 448), amax_t = max_h |decode(q[t,h])| */
+} moe_requant_mode_t;
+
+/*
+ * fp8_requant_per_tensor_ex -- fp8_requant_per_tensor for e8m0 per-token scales
+ * ([P2 风险与影响 item 3]: the original kernel assumes plain fp32 scales and
+ * does not handle Blackwell e8m0 ones) and with an amax-based per-tensor scale
+ * that maps the largest dequantised value to 448. With MOE_TOKSCALE_F32 and
+ * MOE_REQUANT_MAX_SCALE it computes exactly what fp8_requant_per_tensor does.
+ *   s_tok [T] in s_fmt; workspace: >= 4*T bytes, 16-byte aligned, for
+ *   MOE_REQUANT_AMAX (may be NULL otherwise; needs no initialisation).
+ *   q' = RNE_e4m3(fl32(decode(q) * fl32(s[t] / S))); S = 1 when T = 0 or the
+ *   maximum is 0.
+ * Launches: 1 (max-scale) or 2 (amax: per-row maxima, then the rescale).
+ */
+moe_status_t fp8_requant_per_tensor_ex(
+    const void* q, int64_t ldq, const void* s_tok, moe_tokscale_fmt_t s_fmt, int32_t T,
+    int32_t H, moe_requant_mode_t mode, void* q_out, float* d_scale_out, void* workspace,
+    size_t workspace_bytes, moe_stream_t stream);
 
 /* ------------------------------------------------------------------ */
 /* Status                                                              */

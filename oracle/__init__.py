@@ -34,7 +34,8 @@ _SRC = os.path.join(_HERE, "moeperm_oracle.c")
 _HDR = os.path.join(_HERE, "moeperm_oracle.h")
 _LIB = os.path.join(_HERE, "libmoeperm_oracle.so")
 
-FMT = {"u8": 0, "packed": 1, "f32": 2}
+FMT = {"u8": 0, "packed": 1, "f32pow2": 2, "f32": 3, "mx": 4}
+FMT["f32_pow2"] = 2
 ST_OVERFLOW, ST_LIVE_OVERFLOW, ST_BAD_LAYOUT = 1, 2, 4
 
 _lock = threading.Lock()
@@ -84,6 +85,8 @@ def _declare(L):
         "ref_compact_bound": (i64, [i64, i64, i64]),
         "ref_should_use_masked": (i32, [i64, i64]),
         "ref_quant_row": (None, [vp, i32, i32, vp, vp]),
+        "ref_quant_row_fmt": (None, [vp, i32, i32, i32, vp, vp, vp]),
+        "ref_mx_exponent_array": (None, [vp, i64, vp]),
         "ref_scale_bytes": (i64, [i32, i64, i32, i32]),
         "ref_quant_group": (i32, [vp, i64, i32, i32, i32, i32, i32, vp, vp, i64]),
         "ref_dispatch_compact": (i32, [vp, i64, i32, i32, i32, vp, vp, i32, i32, i32, i32, i32,
@@ -93,6 +96,7 @@ def _declare(L):
         "ref_combine_f64": (None, [vp, i64, vp, vp, i32, i32, i32, vp, vp]),
         "ref_combine_f32": (None, [vp, i64, vp, vp, i32, i32, i32, vp]),
         "ref_requant": (None, [vp, i64, vp, i32, i32, vp, vp]),
+        "ref_requant_ex": (None, [vp, i64, vp, i32, i32, i32, i32, vp, vp]),
         "ref_expand_to_slab": (i32, [vp, i32, i32, i64, vp, i64, vp, i32, i32, i32, i32, i32,
                                      vp, vp, i64, vp]),
         "ref_expand_from_slab": (i32, [vp, i32, i32, vp, i64, vp, i32, i32, i32, i32, i32, vp,
@@ -127,6 +131,24 @@ def group_exponent(amax) -> np.ndarray:
     out = np.empty(a.shape, dtype=np.int32)
     lib().ref_group_exponent_array(_p(a), a.size, _p(out))
     return out
+
+
+def mx_exponent(amax) -> np.ndarray:
+    a = np.ascontiguousarray(amax, dtype=np.float32)
+    out = np.empty(a.shape, dtype=np.int32)
+    lib().ref_mx_exponent_array(_p(a), a.size, _p(out))
+    return out
+
+
+def quant_row_fmt(x_bits: np.ndarray, g: int, fmt: str):
+    """(q bytes [H], scale bytes [G], scale values [G] float32) for any format."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    H = x.size
+    q = np.empty(H, np.uint8)
+    eb = np.empty(H // g, np.uint8)
+    sv = np.empty(H // g, np.float32)
+    lib().ref_quant_row_fmt(_p(x), H, g, FMT[fmt], _p(q), _p(eb), _p(sv))
+    return q, eb, sv
 
 
 def bf16_rne(f: float) -> int:
@@ -168,10 +190,10 @@ def scale_buffer(fmt: str, rows: int, G: int, fill: int = 0xA5, ld: int | None =
             ld >= rows-per-block, rounded up to 4 by default.
     Returns (array, ld).
     """
-    if fmt == "u8":
+    if fmt in ("u8", "mx"):
         ld = G if ld is None else ld
         return np.full((rows, ld), fill, np.uint8), ld
-    if fmt == "f32":
+    if fmt in ("f32", "f32pow2", "f32_pow2"):
         ld = G if ld is None else ld
         a = np.full((rows, ld), fill, np.uint32).view(np.float32)
         return a, ld
@@ -229,6 +251,16 @@ def requant(q, s_tok, T, H, ldq=None):
     out = np.empty((T, H), np.uint8)
     S = np.zeros(1, np.float32)
     lib().ref_requant(_p(q), ldq, _p(s_tok), T, H, _p(out), _p(S))
+    return out, float(S[0])
+
+
+def requant_ex(q, s_tok, T, H, s_fmt="f32", mode="max_scale", ldq=None):
+    """s_fmt: "f32" or "ue8m0" (uint8 bytes); mode: "max_scale" or "amax"."""
+    ldq = H if ldq is None else ldq
+    out = np.empty((T, H), np.uint8)
+    S = np.zeros(1, np.float32)
+    lib().ref_requant_ex(_p(q), ldq, _p(s_tok), {"f32": 0, "ue8m0": 1}[s_fmt], T, H,
+                         {"max_scale": 0, "amax": 1}[mode], _p(out), _p(S))
     return out, float(S[0])
 
 

@@ -93,6 +93,25 @@ void ref_group_exponent_array(const float* amax, int64_t n, int32_t* out) {
   for (int64_t i = 0; i < n; ++i) out[i] = ref_group_exponent(amax[i]);
 }
 
+/* [OCP MX] E8M0 shared scale of a block of E4M3 elements: the largest power of
+ * two not above amax, divided by 2^8 (448 = 1.75 * 2^8 is the largest E4M3
+ * value, so emax = 8). Elements that then exceed 448 saturate. */
+int32_t ref_mx_exponent(float amax) {
+  double a = (double)amax;
+  if (!(a > 0.0)) return -127;
+  int k = (int)floor(log2(a));                       /* first guess */
+  while (ldexp(1.0, k) > a) --k;                     /* exact fix-ups */
+  while (ldexp(1.0, k + 1) <= a) ++k;
+  int X = k - 8;
+  if (X < -127) X = -127;
+  if (X > 127) X = 127;
+  return X;
+}
+
+void ref_mx_exponent_array(const float* amax, int64_t n, int32_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = ref_mx_exponent(amax[i]);
+}
+
 static double bf16_value(uint16_t b) {
   uint32_t u = (uint32_t)b << 16;
   float f;
@@ -109,9 +128,16 @@ uint16_t ref_bf16_rne(float f) {
   return (uint16_t)(u >> 16);
 }
 
-/* Quantise one row: q = RNE_e4m3(x * 2^-e) per group, byte = e + 127.
- * x * 2^-e is exact in double. */
-void ref_quant_row(const uint16_t* x, int32_t H, int32_t g, uint8_t* q, uint8_t* ebytes) {
+/* Quantise one row in any format.
+ *  power-of-two formats (U8, PACKED, F32_POW2): e = ref_group_exponent(amax),
+ *    q = RNE_e4m3(x * 2^-e) (exact product), byte e + 127, value 2^e;
+ *  MX_E8M0: X = ref_mx_exponent(amax), q = RNE_e4m3(x * 2^-X) saturated,
+ *    byte X + 127, value 2^X;
+ *  F32: s = fl32(max(amax, 1e-10f) / 448) (one IEEE fp32 division), q =
+ *    RNE_e4m3(fl32(x / s)) -- the sources do not fix the precision of the
+ *    quotient, so the kernel's (an IEEE fp32 division) is taken; byte 0. */
+void ref_quant_row_fmt(const uint16_t* x, int32_t H, int32_t g, int32_t fmt, uint8_t* q,
+                       uint8_t* ebytes, float* svals) {
   int32_t G = H / g;
   for (int32_t gi = 0; gi < G; ++gi) {
     double amax = 0.0;
@@ -119,11 +145,29 @@ void ref_quant_row(const uint16_t* x, int32_t H, int32_t g, uint8_t* q, uint8_t*
       double a = fabs(bf16_value(x[h]));
       if (a > amax) amax = a;
     }
-    int32_t e = ref_group_exponent((float)amax);  /* amax is a bf16 value: exact in float */
+    if (fmt == REF_FMT_F32) {
+      const float eps = 1e-10f;
+      float a = (float)amax > eps ? (float)amax : eps;
+      float sc = a / 448.0f;                                   /* fp32 division */
+      ebytes[gi] = 0;
+      if (svals) svals[gi] = sc;
+      for (int32_t h = gi * g; h < (gi + 1) * g; ++h) {
+        float v = (float)bf16_value(x[h]) / sc;                /* fp32 division */
+        q[h] = ref_e4m3_encode((double)v);
+      }
+      continue;
+    }
+    int32_t e = (fmt == REF_FMT_MX_E8M0) ? ref_mx_exponent((float)amax)
+                                         : ref_group_exponent((float)amax);
     ebytes[gi] = (uint8_t)(e + 127);
+    if (svals) svals[gi] = (float)ldexp(1.0, e);
     for (int32_t h = gi * g; h < (gi + 1) * g; ++h)
-      q[h] = ref_e4m3_encode(ldexp(bf16_value(x[h]), -e));
+      q[h] = ref_e4m3_encode(ldexp(bf16_value(x[h]), -e));  /* saturates above 448 */
   }
+}
+
+void ref_quant_row(const uint16_t* x, int32_t H, int32_t g, uint8_t* q, uint8_t* ebytes) {
+  ref_quant_row_fmt(x, H, g, REF_FMT_UE8M0_U8, q, ebytes, NULL);
 }
 
 /* ------------------------------------------------------------------ */
@@ -140,7 +184,7 @@ static int32_t g4_of(int32_t G) { return (G + 3) / 4; }
 
 static void put_scale(int32_t fmt, void* s, int64_t ld, int64_t rpb, int32_t G, int64_t row,
                       int32_t gi, uint8_t byte) {
-  if (fmt == REF_FMT_UE8M0_U8) {
+  if (fmt == REF_FMT_UE8M0_U8 || fmt == REF_FMT_MX_E8M0) {
     ((uint8_t*)s)[row * ld + gi] = byte;
   } else if (fmt == REF_FMT_F32_POW2) {
     ((float*)s)[row * ld + gi] = (float)ldexp(1.0, (int)byte - 127);
@@ -160,9 +204,9 @@ static void put_scale_pads(int32_t fmt, void* s, int64_t ld, int64_t rpb, int32_
 /* Copy one scale element (U8: 1 byte, F32: 4 bytes, PACKED: 1 byte of a word). */
 static void copy_scale(int32_t fmt, const void* src, int64_t lds, int64_t rpbs, int64_t srow,
                        void* dst, int64_t ldd, int64_t rpbd, int64_t drow, int32_t G, int32_t gi) {
-  if (fmt == REF_FMT_UE8M0_U8) {
+  if (fmt == REF_FMT_UE8M0_U8 || fmt == REF_FMT_MX_E8M0) {
     ((uint8_t*)dst)[drow * ldd + gi] = ((const uint8_t*)src)[srow * lds + gi];
-  } else if (fmt == REF_FMT_F32_POW2) {
+  } else if (fmt == REF_FMT_F32_POW2 || fmt == REF_FMT_F32) {
     ((float*)dst)[drow * ldd + gi] = ((const float*)src)[srow * lds + gi];
   } else {
     int64_t bs = srow / rpbs, rs = srow % rpbs;
@@ -172,10 +216,17 @@ static void copy_scale(int32_t fmt, const void* src, int64_t lds, int64_t rpbs, 
   }
 }
 
+/* Store group gi's scale of a row: the float value for REF_FMT_F32, else the byte. */
+static void put_group_scale(int32_t fmt, void* s, int64_t ld, int64_t rpb, int32_t G,
+                            int64_t row, int32_t gi, uint8_t byte, float val) {
+  if (fmt == REF_FMT_F32) ((float*)s)[row * ld + gi] = val;
+  else put_scale(fmt, s, ld, rpb, G, row, gi, byte);
+}
+
 int64_t ref_scale_bytes(int32_t fmt, int64_t rows, int32_t H, int32_t g) {
   int32_t G = H / g;
-  if (fmt == REF_FMT_UE8M0_U8) return rows * G;
-  if (fmt == REF_FMT_F32_POW2) return rows * G * 4;
+  if (fmt == REF_FMT_UE8M0_U8 || fmt == REF_FMT_MX_E8M0) return rows * G;
+  if (fmt == REF_FMT_F32_POW2 || fmt == REF_FMT_F32) return rows * G * 4;
   return (int64_t)g4_of(G) * 4 * ((rows + 3) / 4 * 4);
 }
 
@@ -224,9 +275,11 @@ int32_t ref_quant_group(const uint16_t* x, int64_t ldx, int32_t T_cap, int32_t n
   if (n_live < 0) n_live = 0;
   int32_t G = H / g;
   uint8_t eb[4096];
+  float sv[4096];
   for (int32_t t = 0; t < n_live; ++t) {
-    ref_quant_row(x + (int64_t)t * ldx, H, g, xq + (int64_t)t * H, eb);
-    for (int32_t gi = 0; gi < G; ++gi) put_scale(fmt, scales, ld_s, INT64_MAX, G, t, gi, eb[gi]);
+    ref_quant_row_fmt(x + (int64_t)t * ldx, H, g, fmt, xq + (int64_t)t * H, eb, sv);
+    for (int32_t gi = 0; gi < G; ++gi)
+      put_group_scale(fmt, scales, ld_s, INT64_MAX, G, t, gi, eb[gi], sv[gi]);
     put_scale_pads(fmt, scales, ld_s, INT64_MAX, G, t);
   }
   return st;
@@ -265,6 +318,7 @@ int32_t ref_dispatch_compact(const uint16_t* x, int64_t ldx, int32_t T, int32_t 
   int32_t G = H / g;
   uint8_t* qrow = (uint8_t*)malloc((size_t)H);
   uint8_t eb[4096];
+  float sv[4096];
   for (int32_t t = 0; t < T; ++t) {
     int quantised = 0;
     for (int32_t k = 0; k < K; ++k) {
@@ -274,9 +328,10 @@ int32_t ref_dispatch_compact(const uint16_t* x, int64_t ldx, int32_t T, int32_t 
       int64_t row = starts[e] + rank[a];
       src2dst[a] = (int32_t)row;
       if (row_weights) row_weights[row] = topk_weights[a];
-      if (!quantised) { ref_quant_row(x + (int64_t)t * ldx, H, g, qrow, eb); quantised = 1; }
+      if (!quantised) { ref_quant_row_fmt(x + (int64_t)t * ldx, H, g, fmt, qrow, eb, sv); quantised = 1; }
       memcpy(xq + row * H, qrow, (size_t)H);
-      for (int32_t gi = 0; gi < G; ++gi) put_scale(fmt, scales, ld_s, INT64_MAX, G, row, gi, eb[gi]);
+      for (int32_t gi = 0; gi < G; ++gi)
+        put_group_scale(fmt, scales, ld_s, INT64_MAX, G, row, gi, eb[gi], sv[gi]);
       put_scale_pads(fmt, scales, ld_s, INT64_MAX, G, row);
     }
   }
@@ -307,6 +362,7 @@ int32_t ref_dispatch_masked(const uint16_t* x, int64_t ldx, int32_t T, int32_t n
   int32_t G = H / g;
   uint8_t* qrow = (uint8_t*)malloc((size_t)H);
   uint8_t eb[4096];
+  float sv[4096];
   for (int32_t t = 0; t < T; ++t) {
     int quantised = 0;
     for (int32_t k = 0; k < K; ++k) {
@@ -316,9 +372,10 @@ int32_t ref_dispatch_masked(const uint16_t* x, int64_t ldx, int32_t T, int32_t n
       int64_t row = (int64_t)e * cap + rank[a];
       src2dst[a] = (int32_t)row;
       if (row_weights) row_weights[row] = topk_weights[a];
-      if (!quantised) { ref_quant_row(x + (int64_t)t * ldx, H, g, qrow, eb); quantised = 1; }
+      if (!quantised) { ref_quant_row_fmt(x + (int64_t)t * ldx, H, g, fmt, qrow, eb, sv); quantised = 1; }
       memcpy(xq + row * H, qrow, (size_t)H);
-      for (int32_t gi = 0; gi < G; ++gi) put_scale(fmt, scales, ld_s, cap, G, row, gi, eb[gi]);
+      for (int32_t gi = 0; gi < G; ++gi)
+        put_group_scale(fmt, scales, ld_s, cap, G, row, gi, eb[gi], sv[gi]);
       put_scale_pads(fmt, scales, ld_s, cap, G, row);
     }
   }
@@ -390,6 +447,38 @@ void ref_requant(const uint8_t* q, int64_t ldq, const float* s_tok, int32_t T, i
       q_out[(int64_t)t * H + h] = ref_e4m3_encode((double)p);
     }
   }
+}
+
+void ref_requant_ex(const uint8_t* q, int64_t ldq, const void* s_tok, int32_t s_fmt, int32_t T,
+                    int32_t H, int32_t mode, uint8_t* q_out, float* S_out) {
+  float* s = (float*)malloc(sizeof(float) * (size_t)(T > 0 ? T : 1));
+  for (int32_t t = 0; t < T; ++t)
+    s[t] = (s_fmt == 0) ? ((const float*)s_tok)[t]
+                        : (float)ldexp(1.0, (int)((const uint8_t*)s_tok)[t] - 127);
+  float S = 0.0f;
+  for (int32_t t = 0; t < T; ++t) {
+    float v = s[t];
+    if (mode == 1) {
+      double amax = 0.0;
+      for (int32_t h = 0; h < H; ++h) {
+        double a = fabs(ref_e4m3_decode(q[(int64_t)t * ldq + h]));
+        if (a > amax) amax = a;
+      }
+      v = s[t] * (float)amax;                                 /* fp32 product */
+    }
+    if (v > S) S = v;
+  }
+  if (mode == 1) S = S / 448.0f;                              /* fp32 division */
+  *S_out = (S > 0.0f) ? S : 1.0f;
+  for (int32_t t = 0; t < T; ++t) {
+    float r = (S > 0.0f) ? s[t] / S : 0.0f;
+    for (int32_t h = 0; h < H; ++h) {
+      float v = (float)ref_e4m3_decode(q[(int64_t)t * ldq + h]);
+      float p = v * r;
+      q_out[(int64_t)t * H + h] = ref_e4m3_encode((double)p);
+    }
+  }
+  free(s);
 }
 
 /* ------------------------------------------------------------------ */

@@ -40,6 +40,9 @@ extern "C" {
 #define REF_FMT_UE8M0_U8 0     /* uint8 [rows, ld] row-major, byte = e + 127 */
 #define REF_FMT_UE8M0_PACKED 1 /* int32 words, column-major per block, 4 groups/word, LSB first */
 #define REF_FMT_F32_POW2 2     /* float [rows, ld] row-major, value 2^e */
+#define REF_FMT_F32 3          /* float [rows, ld]: s = fl32(max(amax,1e-10)/448), q = RNE(fl32(x/s)) */
+#define REF_FMT_MX_E8M0 4      /* uint8 [rows, ld]: OCP MX rule X = floor(log2 amax) - 8, byte X+127,
+                                  q = RNE_e4m3(x * 2^-X) saturated to +-448 */
 
 /* Data-dependent status bits returned by the layout functions. */
 #define REF_ST_OVERFLOW 1      /* an expert received more rows than its slab capacity */
@@ -56,6 +59,11 @@ void ref_e4m3_decode_array(const uint8_t* c, int64_t n, double* out);
 int32_t ref_group_exponent(float amax);
 void ref_group_exponent_array(const float* amax, int64_t n, int32_t* out);
 
+/* OCP MX shared exponent for E4M3 elements: floor(log2(amax)) - 8, clamped to
+ * [-127, 127]; amax = 0 gives -127. */
+int32_t ref_mx_exponent(float amax);
+void ref_mx_exponent_array(const float* amax, int64_t n, int32_t* out);
+
 /* fp32 -> bf16, round to nearest even. */
 uint16_t ref_bf16_rne(float f);
 
@@ -65,6 +73,11 @@ int32_t ref_should_use_masked(int64_t E, int64_t L);
 
 /* Quantise one bf16 row of H elements in groups of g: q[H] bytes, ebytes[H/g]. */
 void ref_quant_row(const uint16_t* x, int32_t H, int32_t g, uint8_t* q, uint8_t* ebytes);
+/* The same for any format: per group the stored scale as a float (2^e for the
+ * power-of-two formats, amax/448 for REF_FMT_F32) and its byte (e + 127, or 0
+ * for REF_FMT_F32). */
+void ref_quant_row_fmt(const uint16_t* x, int32_t H, int32_t g, int32_t fmt, uint8_t* q,
+                       uint8_t* ebytes, float* svals);
 
 /* Scale bytes required for `rows` rows (packed: rows rounded up to 4). */
 int64_t ref_scale_bytes(int32_t fmt, int64_t rows, int32_t H, int32_t g);
@@ -101,6 +114,14 @@ void ref_combine_f32(const uint16_t* y, int64_t ldy, const int32_t* src2dst,
 /* [P2] per-token -> per-tensor e4m3 requant. Returns nothing; writes S. */
 void ref_requant(const uint8_t* q, int64_t ldq, const float* s_tok, int32_t T, int32_t H,
                  uint8_t* q_out, float* S_out);
+
+/* [P2] requant variants. s_fmt: 0 = fp32 per-token scales, 1 = e8m0 bytes
+ * (scale 2^(b - 127)). mode: 0 = S = max_t s[t]; 1 = S = fl32(max_t fl32(s[t] *
+ * amax_t) / 448) with amax_t = max_h |decode(q[t, h])| (the per-tensor scale
+ * that maps the largest dequantised value to 448). Then, as ref_requant,
+ * q' = RNE_e4m3(fl32(decode(q) * fl32(s[t] / S))); S = 1 and r = 0 when S is 0. */
+void ref_requant_ex(const uint8_t* q, int64_t ldq, const void* s_tok, int32_t s_fmt, int32_t T,
+                    int32_t H, int32_t mode, uint8_t* q_out, float* S_out);
 
 /* [P3] expanded psum layout -> masked slab. Returns status bits. */
 int32_t ref_expand_to_slab(const uint8_t* exp, int32_t elem_bytes, int32_t H, int64_t R,

@@ -39,10 +39,14 @@ def test_host_helpers_match_oracle(mp, ref):
         assert mp.moe_compact_bound(A, L, b) == ref.compact_bound(A, L, b)
     for E, L in [(256, 32), (256, 33), (8, 8), (64, 16)]:
         assert mp.moe_should_use_masked(E, L) == ref.should_use_masked(E, L)
-    for fmt, rows, H, g in [("u8", 112, 7168, 32), ("packed", 98048, 7168, 128), ("f32", 5, 640, 128),
+    for fmt, rows, H, g in [("u8", 112, 7168, 32), ("packed", 98048, 7168, 128), ("f32pow2", 5, 640, 128),
                             ("packed", 13, 640, 128), ("u8", 0, 7168, 32)]:
         assert mp.moe_scale_bytes(fmt, rows, H, g) == ref.scale_bytes(fmt, rows, H, g)
-    assert mp.moe_scale_bytes("packed", 10, 7168, 32) == 0      # unsupported pair
+    for fmt, rows, H, g in [("f32", 7, 640, 128), ("mx", 112, 7168, 32)]:
+        assert mp.moe_scale_bytes(fmt, rows, H, g) == ref.scale_bytes(fmt, rows, H, g)
+    assert mp.moe_scale_bytes("packed", 10, 7168, 32) == 0      # unsupported pairs
+    assert mp.moe_scale_bytes("mx", 10, 7168, 128) == 0
+    assert mp.moe_scale_bytes("f32", 10, 7168, 32) == 0
     assert mp.moe_workspace_bytes(8192, 8, 256) >= 256 + 16 * 256 * 4
 
 

@@ -147,8 +147,10 @@ def test_e4m3_convert_exhaustive_via_quant_group(dev, ref):
 
 
 @pytest.mark.parametrize("fmt,g,T,H", [("packed", 128, 50, 640), ("u8", 128, 33, 7168),
-                                       ("f32", 128, 17, 1152), ("u8", 32, 5, 224),
-                                       ("packed", 128, 257, 7168)])
+                                       ("f32pow2", 128, 17, 1152), ("u8", 32, 5, 224),
+                                       ("packed", 128, 257, 7168), ("f32", 128, 33, 7168),
+                                       ("f32", 128, 5, 640), ("mx", 32, 21, 7168),
+                                       ("mx", 32, 3, 224)])
 def test_quant_group_formats(dev, ref, fmt, g, T, H):
     rng = np.random.default_rng(T + H)
     x = synth.normal_bf16(rng, (T, H), outlier_frac=0.02)
@@ -207,7 +209,7 @@ def test_mxfp8_sparse_live_rows_full_size(dev, ref):
 # ---------------------------------------------------------------------------
 
 @pytest.mark.parametrize("seed", range(5))
-@pytest.mark.parametrize("fmt", ["packed", "u8", "f32"])
+@pytest.mark.parametrize("fmt", ["packed", "u8", "f32pow2"])
 def test_dispatch_compact_tiny(dev, ref, seed, fmt):
     d = synth.tiny(seed)
     c = d["cfg"]
@@ -215,7 +217,7 @@ def test_dispatch_compact_tiny(dev, ref, seed, fmt):
                  c["block_e"], c["g"], fmt)
 
 
-@pytest.mark.parametrize("fmt", ["packed", "u8", "f32"])
+@pytest.mark.parametrize("fmt", ["packed", "u8", "f32pow2", "f32"])
 def test_dispatch_compact_tiles_and_ragged_tail(dev, ref, fmt):
     d = synth.prefill(1, T=333, H=1536)
     compact_both(dev, ref, d["x"], d["topk_ids"], d["topk_weights"], 1536, 8, 256, 256, 128, 128, fmt)
@@ -268,9 +270,10 @@ def test_dispatch_compact_degenerate(dev, ref):
     compact_both(dev, ref, x[:0], np.zeros((0, 4), np.int32), w[:0], H, 4, 8, 8, 128, 128, "packed")  # T = 0
 
 
-def test_dispatch_compact_mxfp8_group32(dev, ref):
+@pytest.mark.parametrize("fmt", ["u8", "mx"])
+def test_dispatch_compact_mxfp8_group32(dev, ref, fmt):
     d = synth.mxfp8(2, T_cap=112, n_live=112)
-    compact_both(dev, ref, d["x"], d["topk_ids"], d["topk_weights"], 7168, 8, 256, 256, 128, 32, "u8")
+    compact_both(dev, ref, d["x"], d["topk_ids"], d["topk_weights"], 7168, 8, 256, 256, 128, 32, fmt)
 
 
 # ---------------------------------------------------------------------------
@@ -278,7 +281,7 @@ def test_dispatch_compact_mxfp8_group32(dev, ref):
 # ---------------------------------------------------------------------------
 
 @pytest.mark.parametrize("seed", range(3))
-@pytest.mark.parametrize("fmt", ["packed", "u8"])
+@pytest.mark.parametrize("fmt", ["packed", "u8", "f32"])
 def test_dispatch_masked_decode(dev, ref, seed, fmt):
     d = synth.decode(seed)
     c = d["cfg"]
@@ -295,7 +298,7 @@ def test_dispatch_masked_overflow_fails_fast(dev, ref):
     w = synth.softmax_weights(rng, T, K)
     r, d, status = masked_both(dev, ref, x, ids, w, H, K, 8, 4, 40, 128, "packed")
     assert dev.moe_status_sync(status) == dev.MOE_ERR_OVERFLOW
-    masked_both(dev, ref, x, ids, w, H, K, 8, 4, 64, 128, "f32")   # exactly at capacity
+    masked_both(dev, ref, x, ids, w, H, K, 8, 4, 64, 128, "f32pow2")   # exactly at capacity
 
 
 def test_dispatch_masked_live_tokens(dev, ref):
@@ -447,7 +450,7 @@ def test_repack_build_layout_cases(dev, ref, counts, eb):
     assert bool(st & ref.ST_OVERFLOW) == any(cnt > cap for cnt in counts)
 
 
-@pytest.mark.parametrize("fmt", ["packed", "u8", "f32"])
+@pytest.mark.parametrize("fmt", ["packed", "u8", "f32pow2", "f32"])
 def test_repack_config_fp8_with_quantizer_scales(dev, ref, fmt):
     """Requant/repack config: 64 experts, 128-aligned psum over 4096 expanded
     rows, e4m3 payload and scales made by each side's own quantiser."""
@@ -475,6 +478,24 @@ def test_repack_config_fp8_with_quantizer_scales(dev, ref, fmt):
     # overflow: capacity one block below the largest expert
     st, _, _ = repack_both(dev, ref, exp, 1, H, psum, L, align, cap - 128, fmt=fmt, g=g, exp_sc=esc, ld_es=ld_es)
     assert st & ref.ST_OVERFLOW
+
+
+def test_repack_mx_group32_scales(dev, ref):
+    """OCP MX (group 32) scales through expanded -> slab -> expanded, H = 224
+    (7 groups: not a multiple of 4)."""
+    H, g, align, cap = 224, 32, 8, 16
+    counts = [5, 0, 16, 3, 9]
+    psum, starts, R = build_layout(counts, align)
+    rng = np.random.default_rng(31)
+    x = synth.normal_bf16(rng, (R, H), outlier_frac=0.05)
+    exp = np.zeros((R, H), np.uint8)
+    esc, ld_es = ref.scale_buffer("mx", R, H // g, fill=0)
+    ref.quant_group(x, R, R, H, g, "mx", exp, esc, ld_es)
+    gq = dev.quant_group(bf16_dev(x), group_size=g, scale_fmt="mx")
+    torch.cuda.synchronize()
+    assert_same("gpu mx payload", to_host(gq["xq"], exp), exp)
+    assert_same("gpu mx scales", to_host(gq["scales"], esc), esc)
+    repack_both(dev, ref, exp, 1, H, psum, len(counts), align, cap, fmt="mx", g=g, exp_sc=esc, ld_es=ld_es)
 
 
 def test_repack_weighted_bf16(dev, ref):
@@ -535,6 +556,27 @@ def test_requant_edge_cases(dev, ref):
     assert dev.fp8_requant_per_tensor(None, 16, None, 0, 16, None, dS) == 0
     torch.cuda.synchronize()
     assert float(dS.item()) == 1.0
+
+
+@pytest.mark.parametrize("s_fmt,mode", [("f32", "max_scale"), ("f32", "amax"), ("ue8m0", "max_scale"),
+                                        ("ue8m0", "amax")])
+@pytest.mark.parametrize("T,H", [(4096, 7168), (37, 1040)])
+def test_requant_ex(dev, ref, s_fmt, mode, T, H):
+    d = synth.requant(7, T=T, H=H)
+    q = d["q"]
+    if s_fmt == "f32":
+        s = d["s_tok"]
+    else:
+        s = np.random.default_rng(T).integers(100, 150, size=T).astype(np.uint8)
+    want, S = ref.requant_ex(q, s, T, H, s_fmt, mode)
+    out = torch.full((T, H), 0xEE, dtype=torch.uint8, device=DEV)
+    dS = torch.zeros(1, dtype=torch.float32, device=DEV)
+    ws = torch.empty(T, dtype=torch.float32, device=DEV)
+    assert dev.fp8_requant_per_tensor_ex(to_dev(q), H, to_dev(s), s_fmt, T, H, mode, out, dS, ws,
+                                         ws.numel() * 4) == 0
+    torch.cuda.synchronize()
+    assert_same("requant_ex payload", to_host(out, want), want)
+    assert float(dS.item()) == S
 
 
 # ---------------------------------------------------------------------------

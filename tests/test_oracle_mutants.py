@@ -28,7 +28,7 @@ MUTANTS = [
      ["test_group_exponent_closed_forms", "test_group_exponent_interval_exact"]),
     ("scale_bias", "ebytes[gi] = (uint8_t)(e + 127);", "ebytes[gi] = (uint8_t)(e + 128);",
      ["test_quant_row_against_library", "test_quant_row_zero_group"]),
-    ("eps_changed", "const float eps = 1e-10f;", "const float eps = 1e-12f;",
+    ("eps_changed", "const float eps = 1e-10f;\n  double a", "const float eps = 1e-12f;\n  double a",
      ["test_group_exponent_closed_forms", "test_quant_row_zero_group"]),
     ("scale_sign", "q[h] = ref_e4m3_encode(ldexp(bf16_value(x[h]), -e));",
      "q[h] = ref_e4m3_encode(ldexp(bf16_value(x[h]), e));", ["test_quant_row_against_library"]),

@@ -293,7 +293,7 @@ def check_compact_invariants(ref, r, ids, x, w, H, K, L, b, g, fmt, n_live):
         row = s2d[a]
         assert np.array_equal(r["xq"][row], q)
         assert r["rw"][row] == w.reshape(-1)[a]
-        if fmt == "f32":
+        if fmt == "f32pow2":
             assert np.array_equal(r["sc"][row, :G], np.ldexp(1.0, eb.astype(np.int32) - 127).astype(np.float32))
         else:
             assert np.array_equal(sc_rows[row, :G], eb)
@@ -301,7 +301,7 @@ def check_compact_invariants(ref, r, ids, x, w, H, K, L, b, g, fmt, n_live):
                 assert (sc_rows[row, G:] == 0).all(), "packed pad bytes are zero"
 
 
-@pytest.mark.parametrize("fmt", ["packed", "u8", "f32"])
+@pytest.mark.parametrize("fmt", ["packed", "u8", "f32pow2"])
 def test_dispatch_compact_invariants_random(ref, fmt):
     for seed in range(3):
         d = synth.tiny(seed, T=37, H=640)
@@ -583,7 +583,7 @@ def test_repack_weighted_rows(ref):
     assert (back[~real] == 0xDD).all()
 
 
-@pytest.mark.parametrize("fmt", ["packed", "u8", "f32"])
+@pytest.mark.parametrize("fmt", ["packed", "u8", "f32pow2"])
 def test_repack_scales_from_quantizer(ref, fmt):
     """PR #29525 review lesson: use scales made by the real quantiser, and a
     hidden size whose group count does not divide the packing (H=640 -> 5 groups)."""
@@ -668,3 +668,115 @@ def test_quant_group_live_rows_only(ref):
     assert st & ref.ST_LIVE_OVERFLOW
     st = ref.quant_group(x, 64, 0, H, g, "u8", np.full((64, H), 1, np.uint8), sc, ld)
     assert st == 0
+
+
+# ---------------------------------------------------------------------------
+# Widened formats: plain fp32 group scale, OCP MX floor exponent
+# ---------------------------------------------------------------------------
+
+def test_mx_exponent_closed_forms_and_interval(ref):
+    """OCP MX: X = floor(log2 amax) - 8 (emax of E4M3 is 8): 2^(X+8) <= amax < 2^(X+9)."""
+    assert ref.mx_exponent(np.array([448.0, 256.0, 511.0, 512.0, 1.0, 0.0], np.float32)).tolist() == \
+        [0, 0, 0, 1, -8, -127]
+    a = all_positive_bf16()[::5]
+    X = ref.mx_exponent(a)
+    for av, xv in zip(a.tolist(), X.tolist()):
+        if xv > -127:
+            assert Fraction(2) ** (xv + 8) <= Fraction(av) < Fraction(2) ** (xv + 9)
+        else:
+            assert Fraction(av) < Fraction(2) ** (-118)
+
+
+@pytest.mark.parametrize("H", [224, 7168])
+def test_quant_row_mx_against_library(ref, H):
+    rng = np.random.default_rng(H)
+    g = 32
+    x = graded_row(rng, H, g)
+    q, eb, sv = ref.quant_row_fmt(x, g, "mx")
+    xf = bf16_to_f32(x).reshape(-1, g)
+    X = eb.astype(np.int32) - 127
+    assert np.array_equal(X, ref.mx_exponent(np.abs(xf).max(axis=1)))
+    assert np.array_equal(sv, np.ldexp(1.0, X).astype(np.float32))
+    scaled = np.clip((xf.astype(np.float64) * np.ldexp(1.0, -X)[:, None]), -448, 448).astype(np.float32)
+    assert np.array_equal(q.reshape(-1, g), torch_e4m3(scaled))       # saturating RNE
+    # the block maximum lands in [256, 512) before saturation: some codes are clipped to 448
+    assert (np.abs(xf).max(axis=1) * np.ldexp(1.0, -X) >= 256).all()
+
+
+@pytest.mark.parametrize("g,H", [(128, 640), (128, 7168), (32, 224)])
+def test_quant_row_f32_against_library(ref, g, H):
+    rng = np.random.default_rng(g * H)
+    x = graded_row(rng, H, g)
+    x[:g] = 0                                    # an all-zero group uses the 1e-10 floor
+    q, eb, sv = ref.quant_row_fmt(x, g, "f32")
+    xf = bf16_to_f32(x).reshape(-1, g)
+    s = np.maximum(np.abs(xf).max(axis=1), np.float32(1e-10)) / np.float32(448.0)   # fp32 division
+    assert np.array_equal(sv, s.astype(np.float32))
+    v = np.clip(xf / s[:, None].astype(np.float32), -448, 448).astype(np.float32)   # fp32 division
+    assert np.array_equal(q.reshape(-1, g), torch_e4m3(v))
+
+
+def test_error_study_direct_ue8m0_vs_round_after(ref):
+    """PR #33128 实现拆解 item 3: quantising with an fp32 scale and rounding the
+    scale up to a power of two afterwards misrepresents values by up to 2x;
+    choosing the power of two first (direct UE8M0) keeps the e4m3 rounding
+    error. Measured on N(0,1) rows with 1% outliers x50 (decode workload)."""
+    rng = np.random.default_rng(0)
+    H, g = 7168, 128
+    rows = synth.normal_bf16(rng, (16, H), outlier_frac=0.01)
+    err = {"direct": [], "fp32": [], "round_after": []}
+    for x in rows:
+        xf = bf16_to_f32(x).astype(np.float64).reshape(-1, g)
+        q, eb, _ = ref.quant_row_fmt(x, g, "u8")
+        d = ref.e4m3_decode(q).reshape(-1, g) * np.ldexp(1.0, eb.astype(np.int32) - 127)[:, None]
+        qf, _, s = ref.quant_row_fmt(x, g, "f32")
+        df = ref.e4m3_decode(qf).reshape(-1, g) * s[:, None].astype(np.float64)
+        s_up = np.ldexp(1.0, np.ceil(np.log2(s.astype(np.float64))).astype(np.int32))
+        dr = ref.e4m3_decode(qf).reshape(-1, g) * s_up[:, None]
+        nz = np.abs(xf) > 2.0 ** -6 * np.abs(xf).max(axis=1, keepdims=True)   # normal-range elements
+        for k, dd in (("direct", d), ("fp32", df), ("round_after", dr)):
+            err[k].append(np.max(np.abs(dd - xf)[nz] / np.abs(xf)[nz]))
+    e = {k: max(v) for k, v in err.items()}
+    assert e["direct"] <= 2.0 ** -4 + 1e-12      # half an e4m3 ulp, relative
+    assert e["fp32"] <= 2.0 ** -4 + 1e-12
+    assert e["round_after"] > 0.5                # values land up to 2x off
+
+
+# ---------------------------------------------------------------------------
+# Widened requant: amax-based per-tensor scale, e8m0 per-token scales
+# ---------------------------------------------------------------------------
+
+def test_requant_ex_max_scale_f32_equals_requant(ref):
+    d = synth.requant(3, T=50, H=272)
+    a, Sa = ref.requant(d["q"], d["s_tok"], 50, 272)
+    b, Sb = ref.requant_ex(d["q"], d["s_tok"], 50, 272, "f32", "max_scale")
+    assert Sa == Sb and np.array_equal(a, b)
+
+
+def test_requant_ex_amax_mode_against_library(ref):
+    d = synth.requant(4, T=64, H=256)
+    q, s = d["q"], d["s_tok"]
+    out, S = ref.requant_ex(q, s, 64, 256, "f32", "amax")
+    dq = ref.e4m3_decode(q).astype(np.float32)
+    amax = np.abs(dq).max(axis=1).astype(np.float32)
+    P = (s * amax).astype(np.float32)                                   # fp32 products
+    assert S == float(np.float32(P.max()) / np.float32(448.0))           # fp32 division
+    r = (s / np.float32(S)).astype(np.float32)
+    v = np.clip((dq * r[:, None]).astype(np.float32), -448, 448)
+    assert np.array_equal(out, torch_e4m3(v))
+    t = int(np.argmax(P))
+    assert np.abs(ref.e4m3_decode(out[t])).max() == 448.0, "the largest value maps to 448"
+
+
+def test_requant_ex_ue8m0_scales_are_exact_powers(ref):
+    rng = np.random.default_rng(6)
+    T, H = 40, 64
+    q = synth.to_e4m3_bits(np.clip(rng.standard_normal((T, H)).astype(np.float32) * 64, -448, 448))
+    b = rng.integers(110, 140, size=T).astype(np.uint8)
+    out, S = ref.requant_ex(q, b, T, H, "ue8m0", "max_scale")
+    assert S == 2.0 ** (int(b.max()) - 127)
+    # r_t = 2^(b_t - b_max) exactly: the requant is an exact power-of-two rescale + RNE
+    v = ref.e4m3_decode(q) * np.ldexp(1.0, b.astype(np.int32) - int(b.max()))[:, None]
+    assert np.array_equal(out, torch_e4m3(v.astype(np.float32)))
+    same = ref.requant_ex(q, np.ldexp(1.0, b.astype(np.int32) - 127).astype(np.float32), T, H, "f32", "max_scale")
+    assert np.array_equal(same[0], out) and same[1] == S
