@@ -548,6 +548,59 @@ def other_rows(mp, dev, flush):
     return res
 
 
+def layout_sweep(args):
+    """Compact vs masked dispatch cost of these kernels over (T, L) -- the
+    layout question the PR #33128 review raises (compact slower than masked
+    below ~8192 tokens with 128 local experts), restricted to the permute /
+    quantise step (no GEMM). Uniform top-8 routing over 256 experts of which
+    the first L are local; the masked capacity is the largest expert's count
+    rounded up to 128. One JSON line per point."""
+    import torch
+    import combine_fp8_quant_gb300 as mp
+    from combine_fp8_quant_gb300 import build as cuda_build
+    cuda_build.build()
+    mp.load()
+    dev = torch.device("cuda:0")
+    flush = L2Flush(dev)
+    H, K, E, g = 7168, 8, 256, 128
+    for T in (128, 512, 2048, 8192):
+        rng = np.random.default_rng(T)
+        x = torch.from_numpy(synth.normal_bf16(rng, (T, H)).view(np.int16)).to(dev).view(torch.bfloat16)
+        ids_np = synth.uniform_topk(rng, T, E, K)
+        ids = torch.from_numpy(ids_np).to(dev)
+        for L in (32, 128, 256):
+            cnt = np.bincount(ids_np[ids_np < L].ravel(), minlength=L)
+            cap = max(128, int(-(-cnt.max() // 128) * 128))
+            ws = mp.Workspace(T, K, L, dev)
+            st = torch.zeros(1, dtype=torch.int32, device=dev)
+            bound = mp.moe_compact_bound(T * K, L, 128)
+            xq = torch.empty((bound, H), dtype=torch.uint8, device=dev)
+            sc, ld = mp.scale_tensor("packed", bound, H, g, dev)
+            mi = torch.empty(bound, dtype=torch.int32, device=dev)
+            s2d = torch.empty((T, K), dtype=torch.int32, device=dev)
+            c3 = [torch.empty(L, dtype=torch.int32, device=dev) for _ in range(3)]
+            tot = torch.empty(1, dtype=torch.int32, device=dev)
+            xqm = torch.empty((L, cap, H), dtype=torch.uint8, device=dev)
+            scm, ldm = mp.scale_tensor("packed", L * cap, H, g, dev, blocks=L)
+            mm = torch.empty(L, dtype=torch.int32, device=dev)
+
+            def compact():
+                assert mp.moe_dispatch_compact(x, H, T, None, H, ids, None, K, E, L, 128, g, "packed",
+                                               xq, sc, ld, mi, bound, s2d, *c3, tot, None, ws.buf,
+                                               ws.nbytes, st) == 0
+
+            def masked():
+                assert mp.moe_dispatch_masked(x, H, T, None, H, ids, None, K, E, L, cap, g, "packed",
+                                              xqm, scm, ldm, mm, s2d, None, ws.buf, ws.nbytes, st) == 0
+            uc, um = time_call(compact, flush), time_call(masked, flush)
+            torch.cuda.synchronize()
+            assert mp.moe_status_sync(st) == 0
+            print(json.dumps({"layout_sweep": True, "T": T, "L": L, "E": E, "kept_slots": int(cnt.sum()),
+                              "compact_rows": bound, "masked_rows": L * cap, "compact_us": uc,
+                              "masked_us": um, "masked_over_compact": um / uc}), flush=True)
+            del xq, sc, mi, xqm, scm
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -559,7 +612,12 @@ def main():
                          "baseline); used for profiler captures")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override T of the prefill workload (profiling smaller cases)")
+    ap.add_argument("--layout-sweep", action="store_true",
+                    help="compact vs masked dispatch cost over (T, L); one JSON line per point")
     args = ap.parse_args()
+    if args.layout_sweep:
+        layout_sweep(args)
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmoeperm.so")
 UNITS = ["api.cu", "route_plan.cu", "quant_scatter.cu", "combine.cu", "repack.cu", "requant.cu",
-         "noalloc.cu"]
+         "noalloc.cu", "dispatch_small.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "-Xptxas", "-v",
          "--expt-relaxed-constexpr", "-I" + os.path.join(ROOT, "include")]

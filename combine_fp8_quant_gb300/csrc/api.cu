@@ -83,6 +83,18 @@ moe_status_t run_dispatch(const DispatchCommon& c, int mode, int32_t block_e, in
   const int sms = num_sms_cached();
   if (sms <= 0) return MOE_ERR_CUDA;
   const int64_t A = (int64_t)c.T * c.K;
+  if (A <= kSmallSlots) {  // latency-bound: one launch, no workspace traffic
+    ScatterArgs sa{};
+    sa.x = static_cast<const uint16_t*>(c.x); sa.ldx = c.ldx; sa.T = c.T;
+    sa.d_num_tokens = c.d_num_tokens; sa.H = c.H; sa.ids = c.ids; sa.w = c.w;
+    sa.K = c.K; sa.L = c.L; sa.mode = mode; sa.block_e = block_e; sa.cap = cap;
+    sa.xq = static_cast<uint8_t*>(c.xq); sa.scales = c.scales; sa.ld_s = c.ld_s;
+    sa.src2dst = c.src2dst; sa.row_weights = c.row_weights;
+    sa.m_indices = m_indices; sa.bound = bound;
+    sa.counts = counts; sa.starts = starts; sa.psum = psum; sa.total = total;
+    sa.masked_m = masked_m; sa.status = d_status;
+    return cuda_status(launch_dispatch_small(sa, c.g, c.fmt, sms, stream));
+  }
   const int S = route_plan_S(A, c.L);
   const int64_t nchunks = route_nchunks(A, S);
   int32_t* table = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(c.ws) + kWsHeader);

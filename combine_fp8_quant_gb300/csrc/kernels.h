@@ -61,6 +61,12 @@ struct ScatterArgs {
 cudaError_t launch_quant_scatter(const ScatterArgs& a, int g, int fmt, int num_sms,
                                  bool after_route_plan, cudaStream_t s);
 
+// Single-launch dispatch for small problems (T*K <= kSmallSlots): every CTA
+// ranks all slots itself; no chunk table, no route-plan launch.
+constexpr int64_t kSmallSlots = 4096;
+cudaError_t launch_dispatch_small(const ScatterArgs& a, int g, int fmt, int num_sms,
+                                  cudaStream_t s);
+
 // ---------------------------------------------------------------------------
 // Combine
 // ---------------------------------------------------------------------------

@@ -217,9 +217,10 @@ def test_dispatch_compact_tiny(dev, ref, seed, fmt):
                  c["block_e"], c["g"], fmt)
 
 
+@pytest.mark.parametrize("T", [333, 613])   # 2664 slots: one-launch path; 4904: two-launch path
 @pytest.mark.parametrize("fmt", ["packed", "u8", "f32pow2", "f32"])
-def test_dispatch_compact_tiles_and_ragged_tail(dev, ref, fmt):
-    d = synth.prefill(1, T=333, H=1536)
+def test_dispatch_compact_tiles_and_ragged_tail(dev, ref, fmt, T):
+    d = synth.prefill(1, T=T, H=1536)
     compact_both(dev, ref, d["x"], d["topk_ids"], d["topk_weights"], 1536, 8, 256, 256, 128, 128, fmt)
 
 
@@ -288,6 +289,24 @@ def test_dispatch_masked_decode(dev, ref, seed, fmt):
     assert ref.should_use_masked(c["E"], c["L"])
     masked_both(dev, ref, d["x"], d["topk_ids"], d["topk_weights"], c["H"], c["K"], c["E"], c["L"],
                 c["cap"], c["g"], fmt)
+
+
+@pytest.mark.parametrize("fmt", ["packed", "u8", "f32"])
+def test_dispatch_masked_two_launch_path(dev, ref, fmt):
+    """T*K = 5600 slots (> 4096): route-plan launch + scatter launch."""
+    d = synth.decode(5, T=700)
+    x = d["x"][:, :1024].copy()
+    masked_both(dev, ref, x, d["topk_ids"], d["topk_weights"], 1024, 8, 256, 32, 128, 128, fmt)
+
+
+def test_dispatch_masked_overflow_two_launch_path(dev, ref):
+    rng = np.random.default_rng(18)
+    T, K, H = 600, 8, 256
+    x = synth.normal_bf16(rng, (T, H))
+    ids = synth.uniform_topk(rng, T, 16, K)      # ~300 slots per local expert
+    w = synth.softmax_weights(rng, T, K)
+    r, d, status = masked_both(dev, ref, x, ids, w, H, K, 16, 8, 256, 128, "packed")
+    assert dev.moe_status_sync(status) == dev.MOE_ERR_OVERFLOW
 
 
 def test_dispatch_masked_overflow_fails_fast(dev, ref):
