@@ -414,17 +414,21 @@ def kernel_source_sha(files):
 
 
 def load_traffic(which):
-    """DRAM bytes (read + write) per launch of a kernel, from the committed ncu
-    summary profiles/traffic.json -- null when absent or when the kernel's
-    source has changed since the counters were taken."""
-    p = os.path.join(ROOT, "profiles", "traffic.json")
+    """DRAM bytes (read + write) per launch of a kernel (per call, for the
+    two-launch dispatch) from the committed ncu summary
+    profiles/dram_traffic_prefill.txt -- null when absent or when a source
+    file of the kernel has changed since the counters were taken."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic_prefill.txt")
     if not os.path.exists(p):
         return None
-    with open(p) as f:
-        d = json.load(f).get(which)
-    if not d or d.get("source_sha") != kernel_source_sha(d.get("sources", [])):
-        return None
-    return d.get("bytes_per_launch")
+    for line in open(p):
+        parts = line.split()
+        if len(parts) == 4 and not line.startswith("#") and parts[0] == which:
+            files = parts[3].split(",")
+            if parts[2] != kernel_source_sha(files):
+                return None
+            return int(parts[1])
+    return None
 
 
 def time_call(fn, flush, reps=20):

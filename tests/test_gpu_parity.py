@@ -651,3 +651,74 @@ def test_graph_capture_replay_new_routing(dev, ref):
         want = ref.combine_f32(ynp, rs2d, dn["topk_weights"], T, K, H)
         assert_same("graph combine", to_host(comb.view(torch.int16), want), want)
     assert int(st.item()) == 0
+
+
+# ---------------------------------------------------------------------------
+# Full size, in the benchmark's launch configuration (prefill workload)
+# ---------------------------------------------------------------------------
+
+def test_prefill_full_size_sampled(dev, ref):
+    """T = 8192, H = 7168, 256 local experts, top-8 Zipf routing, block_e 128,
+    packed UE8M0 -- the call bench.py times. The layout does not depend on H,
+    so the oracle run on the first 128 columns gives the full layout and the
+    first group of every row bit-exactly; sampled tokens are checked over the
+    whole row (payload, all 56 scales) and through the combine."""
+    d = synth.prefill(0)
+    c = d["cfg"]
+    T, H, K, E, L, b, g = c["T"], c["H"], c["K"], c["E"], c["L"], c["block_e"], c["g"]
+    x, ids, w = d["x"], d["topk_ids"], d["topk_weights"]
+    out = dev.dispatch_compact(bf16_dev(x), to_dev(ids), to_dev(w), E, L, block_e=b, group_size=g,
+                               scale_fmt="packed")
+    torch.cuda.synchronize()
+    bound = out["bound"]
+    # oracle on the first group of columns (ldx = H, width 128)
+    rxq = np.zeros((bound, 128), np.uint8)
+    rsc, rld = ref.scale_buffer("packed", bound, 1, fill=0)
+    rmi = np.zeros(bound, np.int32)
+    rs2d = np.zeros((T, K), np.int32)
+    rc, rs, rp = (np.zeros(L, np.int32) for _ in range(3))
+    rt = np.zeros(1, np.int32)
+    rrw = np.full(bound, np.nan, np.float32)
+    ref.dispatch_compact(x, T, T, 128, ids, w, K, L, b, g, "packed", rxq, rsc, rld, rmi, bound, rs2d,
+                         rc, rs, rp, rt, rrw, ldx=H)
+    s2d = out["src2dst"].cpu().numpy()
+    assert np.array_equal(s2d, rs2d)
+    assert np.array_equal(out["m_indices"].cpu().numpy(), rmi)
+    assert np.array_equal(out["counts"].cpu().numpy(), rc)
+    assert np.array_equal(out["starts"].cpu().numpy(), rs)
+    assert np.array_equal(out["psum"].cpu().numpy(), rp)
+    assert int(out["total"].item()) == int(rt[0])
+    rows = s2d[s2d >= 0]
+    xq = out["xq"]
+    got_g0 = xq[torch.from_numpy(rows).to(DEV).long(), :128].cpu().numpy()
+    assert np.array_equal(got_g0, rxq[rows])
+    rw = out["row_weights"].cpu().numpy()
+    assert np.array_equal(rw[rows], rrw[rows])
+    sc_words = out["scales"].cpu().numpy().reshape(-1, out["ld_s"])       # [G4, ld] int32
+    g0 = (sc_words[0, rows] & 0xFF).astype(np.uint8)
+    want_g0 = rsc.view(np.int32).reshape(-1, rld)[0, rows].astype(np.uint32) & 0xFF
+    assert np.array_equal(g0, want_g0.astype(np.uint8))
+    # sampled tokens: whole rows and all scales
+    rng = np.random.default_rng(0)
+    for t in rng.choice(T, size=24, replace=False):
+        q, eb = ref.quant_row(x[t], g)
+        for k in range(K):
+            row = s2d[t, k]
+            assert row >= 0
+            assert np.array_equal(xq[row].cpu().numpy(), q)
+            words = sc_words[:, row].astype(np.uint32)
+            got_eb = np.stack([(words >> (8 * i)) & 0xFF for i in range(4)], axis=1).reshape(-1)[:H // g]
+            assert np.array_equal(got_eb.astype(np.uint8), eb)
+    # combine of sampled tokens against the fp32-FMA twin
+    gen = torch.Generator(device=DEV)
+    gen.manual_seed(11)
+    y = torch.randn((bound, H), generator=gen, device=DEV).to(torch.bfloat16)
+    o = dev.combine(y, out["src2dst"], to_dev(w))
+    torch.cuda.synchronize()
+    sample = rng.choice(T, size=32, replace=False)
+    for t in sample:
+        yr = y[torch.from_numpy(s2d[t]).to(DEV).long()].view(torch.int16).cpu().numpy().view(np.uint16)
+        want = ref.combine_f32(np.ascontiguousarray(yr), np.arange(K, dtype=np.int32)[None, :],
+                               np.ascontiguousarray(w[t:t + 1]), 1, K, H)
+        got = o[t].view(torch.int16).cpu().numpy().view(np.uint16)
+        assert np.array_equal(got, want[0])
