@@ -1,5 +1,5 @@
 // dispatch_small.cu -- the whole dispatch in ONE launch for small problems
-// (T*K <= 4096 slots: decode batches), where launch latency, not bandwidth,
+// (T*K <= 2048 slots: decode batches), where launch latency, not bandwidth,
 // sets the time.
 //
 // Computes exactly what route_plan.cu + quant_scatter.cu compute (same
@@ -326,7 +326,7 @@ cudaError_t launch_f(const ScatterArgs& a, int num_sms, cudaStream_t s) {
   if (A <= 256) return launch_s<GSZ, FMT, 1>(a, num_sms, s);
   if (A <= 1024) return launch_s<GSZ, FMT, 4>(a, num_sms, s);
   if (A <= 2048) return launch_s<GSZ, FMT, 8>(a, num_sms, s);
-  return launch_s<GSZ, FMT, 16>(a, num_sms, s);
+  return launch_s<GSZ, FMT, 16>(a, num_sms, s);  // only if the threshold is raised (<= 4096)
 }
 
 }  // namespace

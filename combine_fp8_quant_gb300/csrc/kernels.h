@@ -62,8 +62,13 @@ cudaError_t launch_quant_scatter(const ScatterArgs& a, int g, int fmt, int num_s
                                  bool after_route_plan, cudaStream_t s);
 
 // Single-launch dispatch for small problems (T*K <= kSmallSlots): every CTA
-// ranks all slots itself; no chunk table, no route-plan launch.
-constexpr int64_t kSmallSlots = 4096;
+// ranks all slots itself; no chunk table, no route-plan launch. Measured on
+// GB300 (H = 7168, top-8): faster than the two-launch plan up to 2048 slots,
+// equal at 2048, slower at 4096 (the redundant ranking grows with T*K).
+#ifndef MOEPERM_SMALL_SLOTS
+#define MOEPERM_SMALL_SLOTS 2048
+#endif
+constexpr int64_t kSmallSlots = MOEPERM_SMALL_SLOTS;
 cudaError_t launch_dispatch_small(const ScatterArgs& a, int g, int fmt, int num_sms,
                                   cudaStream_t s);
 

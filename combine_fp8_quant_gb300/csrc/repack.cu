@@ -10,10 +10,10 @@
 //   psum inconsistent with the R expanded rows -> MOE_STATUS_BAD_LAYOUT.
 //
 // Design: a fixed worker pool (grid = SMs x resident CTAs, capped by R) walks
-// the R expanded rows, so the launch never depends on the routing; each CTA
-// finds a row's expert by binary search over the segment starts held in shared
-// memory and copies the row with 16-byte vectors (all loads of a pass in
-// flight before the stores). Scales follow each side's own layout (stride
+// the R expanded rows, one row per warp, so the launch never depends on the
+// routing; a warp finds its row's expert by binary search over the segment
+// starts held in shared memory and copies the row with 16-byte vectors, up to
+// 16 per lane issued before the first store (a 7 KB e4m3 row in one pass). Scales follow each side's own layout (stride
 // aware): row-major bytes / floats, or column-major packed UE8M0 words with
 // one block per expert on the slab side; pad bytes of the last packed word are
 // cleared.
@@ -24,14 +24,16 @@ namespace moeperm {
 
 namespace {
 
-constexpr int kThreads = 128;
-constexpr int kUnroll = 4;
+constexpr int kThreads = 256;
+constexpr int kPass = 16;   // 16-byte chunks per lane in flight
 
 __global__ void __launch_bounds__(kThreads) repack_kernel(RepackArgs p) {
   extern __shared__ int32_t sm[];
   int32_t* s_start = sm;
   int32_t* s_psum = sm + p.L;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int gwarp = (int)((blockIdx.x * kThreads + threadIdx.x) >> 5);
+  const int nwarps = (int)((gridDim.x * kThreads) >> 5);
   const int L = p.L;
   for (int e = tid; e < L; e += kThreads) {
     const int pe = __ldg(p.psum + e);
@@ -55,7 +57,7 @@ __global__ void __launch_bounds__(kThreads) repack_kernel(RepackArgs p) {
   const int G = p.G, G4 = (G + 3) / 4;
   const bool scales = p.src_scales != nullptr && p.dst_scales != nullptr && G > 0;
   const bool weighted = !p.to_slab && p.row_weights != nullptr && p.elem_bytes == 2;
-  for (int64_t r = blockIdx.x; r < p.R; r += gridDim.x) {
+  for (int64_t r = gwarp; r < p.R; r += nwarps) {
     int lo = 0, hi = L - 1;  // largest e with start[e] <= r
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
@@ -63,23 +65,23 @@ __global__ void __launch_bounds__(kThreads) repack_kernel(RepackArgs p) {
     }
     const int e = lo;
     const bool real = r < s_psum[e] && r >= s_start[e];
-    if (!p.to_slab && p.m_indices != nullptr && tid == 0) p.m_indices[r] = real ? e : -1;
+    if (!p.to_slab && p.m_indices != nullptr && lane == 0) p.m_indices[r] = real ? e : -1;
     const int64_t j = r - s_start[e];
     if (!real || j >= p.cap) continue;
     const int64_t srow = (int64_t)e * p.cap + j;  // slab row
     const uint8_t* src = p.src + (p.to_slab ? r : srow) * rowbytes;
     uint8_t* dst = p.dst + (p.to_slab ? srow : r) * rowbytes;
     const float wr = weighted ? __ldg(p.row_weights + r) : 1.0f;
-    for (int c0 = 0; c0 < nch; c0 += kUnroll * kThreads) {
-      uint4 v[kUnroll];
+    for (int c0 = 0; c0 < nch; c0 += 32 * kPass) {
+      uint4 v[kPass];
 #pragma unroll
-      for (int i = 0; i < kUnroll; ++i) {
-        const int c = c0 + i * kThreads + tid;
-        if (c < nch) v[i] = ld_nc_v4(src + (int64_t)c * 16);
+      for (int i = 0; i < kPass; ++i) {
+        const int c = c0 + i * 32 + lane;
+        v[i] = (c < nch) ? ld_nc_v4(src + (int64_t)c * 16) : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
-      for (int i = 0; i < kUnroll; ++i) {
-        const int c = c0 + i * kThreads + tid;
+      for (int i = 0; i < kPass; ++i) {
+        const int c = c0 + i * 32 + lane;
         if (c < nch) {
           uint4 o = v[i];
           if (weighted) {
@@ -96,7 +98,7 @@ __global__ void __launch_bounds__(kThreads) repack_kernel(RepackArgs p) {
       if (p.fmt == kFmtPacked) {
         const uint32_t* s32 = reinterpret_cast<const uint32_t*>(p.src_scales);
         uint32_t* d32 = reinterpret_cast<uint32_t*>(p.dst_scales);
-        for (int w = tid; w < G4; w += kThreads) {
+        for (int w = lane; w < G4; w += 32) {
           const int64_t xw = (int64_t)w * (p.to_slab ? p.ld_src_s : p.ld_dst_s) + r;
           const int64_t sw = (int64_t)e * G4 * (p.to_slab ? p.ld_dst_s : p.ld_src_s) +
                              (int64_t)w * (p.to_slab ? p.ld_dst_s : p.ld_src_s) + j;
@@ -109,13 +111,13 @@ __global__ void __launch_bounds__(kThreads) repack_kernel(RepackArgs p) {
         uint8_t* d8 = reinterpret_cast<uint8_t*>(p.dst_scales);
         const int64_t so = (p.to_slab ? r : srow) * p.ld_src_s;
         const int64_t dof = (p.to_slab ? srow : r) * p.ld_dst_s;
-        for (int gi = tid; gi < G; gi += kThreads) d8[dof + gi] = __ldg(s8 + so + gi);
+        for (int gi = lane; gi < G; gi += 32) d8[dof + gi] = __ldg(s8 + so + gi);
       } else {
         const float* sf = reinterpret_cast<const float*>(p.src_scales);
         float* df = reinterpret_cast<float*>(p.dst_scales);
         const int64_t so = (p.to_slab ? r : srow) * p.ld_src_s;
         const int64_t dof = (p.to_slab ? srow : r) * p.ld_dst_s;
-        for (int gi = tid; gi < G; gi += kThreads) df[dof + gi] = __ldg(sf + so + gi);
+        for (int gi = lane; gi < G; gi += 32) df[dof + gi] = __ldg(sf + so + gi);
       }
     }
   }
@@ -130,7 +132,8 @@ cudaError_t launch_repack(const RepackArgs& a, int num_sms, cudaStream_t s) {
   if (err != cudaSuccess) return err;
   if (per_sm < 1) per_sm = 1;
   int64_t grid = (int64_t)num_sms * per_sm;
-  if (grid > a.R) grid = a.R;
+  const int64_t need = (a.R + kThreads / 32 - 1) / (kThreads / 32);  // one warp per expanded row
+  if (grid > need) grid = need;
   if (grid < 1) grid = 1;
   repack_kernel<<<(unsigned)grid, kThreads, smem, s>>>(a);
   return cudaGetLastError();

@@ -10,10 +10,11 @@
 //   S = 1 if T = 0 or the maximum is 0 (then r = 0)
 //   q_out[t, h] = RNE_e4m3( fl32( decode(q[t, h]) * fl32(s[t] / S) ) )
 //
-// Design: the max-scale mode is one launch. Every CTA first issues its first
-// row's loads, then reduces the T scales itself (float4 / byte loads, L2-
-// resident) while they are in flight, and streams rows: 16 e4m3 bytes per
-// thread per step, widened exactly with cvt.rn.f16x2.e4m3x2, scaled in fp32,
+// Design: the max-scale mode is one launch. Rows go one per warp; each warp
+// first issues all the loads of its first row (up to 16 x 16 bytes per lane),
+// then its CTA reduces the T scales (float4 / byte loads, L2-resident) while
+// they are in flight, and the warp converts and stores: 16 e4m3 bytes per lane
+// per vector, widened exactly with cvt.rn.f16x2.e4m3x2, scaled in fp32,
 // narrowed with cvt.rn.satfinite.e4m3x2.f32. The amax mode adds a first launch
 // that writes fl32(s[t] * amax_t) per row to the workspace (the row maximum is
 // a byte-wise __vmaxu4 of sign-cleared codes: for finite e4m3 the code order is
@@ -83,49 +84,55 @@ __device__ __forceinline__ float reduce_e8m0(const uint8_t* b, int n, float* s_r
   return block_max(m ? e8m0_value(m) : 0.0f, s_red);
 }
 
+// Rows are processed one per warp: a lane issues up to kPass 16-byte loads of
+// its row before the first conversion, so a 7 KB row is fully in flight.
+constexpr int kPass = 16;
+
 // amax mode, launch 1: ws[t] = fl32(s[t] * max_h |decode(q[t, h])|)
 template <int SFMT>
 __global__ void __launch_bounds__(kThreads) requant_rowmax_kernel(RequantArgs p) {
-  __shared__ uint32_t s_red[kThreads / 32];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int lane = threadIdx.x & 31;
+  const int gwarp = (int)((blockIdx.x * kThreads + threadIdx.x) >> 5);
+  const int nwarps = (int)((gridDim.x * kThreads) >> 5);
   const int nch = p.H / 16;
-  for (int t = blockIdx.x; t < p.T; t += gridDim.x) {
+  for (int t = gwarp; t < p.T; t += nwarps) {
     const uint8_t* src = p.q + (int64_t)t * p.ldq;
     uint32_t m = 0;
-    for (int c = tid; c < nch; c += kThreads) {
-      const uint4 v = ld_nc_v4(src + (int64_t)c * 16);
+    for (int c0 = 0; c0 < nch; c0 += 32 * kPass) {
+      uint4 v[kPass];
+#pragma unroll
+      for (int j = 0; j < kPass; ++j) {
+        const int c = c0 + j * 32 + lane;
+        v[j] = (c < nch) ? ld_nc_v4(src + (int64_t)c * 16) : make_uint4(0, 0, 0, 0);
+      }
       const uint32_t k = 0x7F7F7F7Fu;
-      m = __vmaxu4(m, __vmaxu4(__vmaxu4(v.x & k, v.y & k), __vmaxu4(v.z & k, v.w & k)));
+#pragma unroll
+      for (int j = 0; j < kPass; ++j)
+        m = __vmaxu4(m, __vmaxu4(__vmaxu4(v[j].x & k, v[j].y & k), __vmaxu4(v[j].z & k, v[j].w & k)));
     }
     m = max(max(m & 0xFFu, (m >> 8) & 0xFFu), max((m >> 16) & 0xFFu, m >> 24));
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
-    if (lane == 0) s_red[warp] = m;
-    __syncthreads();
-    if (tid == 0) {
-      uint32_t mm = 0;
-      for (int w = 0; w < kThreads / 32; ++w) mm = max(mm, s_red[w]);
-      const float amax = e4m3x2_to_float2(mm).x;
-      p.ws[t] = __fmul_rn(token_scale<SFMT>(p, t), amax);
-    }
-    __syncthreads();
+    if (lane == 0) p.ws[t] = __fmul_rn(token_scale<SFMT>(p, t), e4m3x2_to_float2(m).x);
   }
 }
 
 template <int SFMT, int MODE>
 __global__ void __launch_bounds__(kThreads) requant_kernel(RequantArgs p) {
   __shared__ float s_red[kThreads / 32];
-  const int tid = threadIdx.x;
+  const int lane = threadIdx.x & 31, tid = threadIdx.x;
+  const int gwarp = (int)((blockIdx.x * kThreads + threadIdx.x) >> 5);
+  const int nwarps = (int)((gridDim.x * kThreads) >> 5);
   const int nch = p.H / 16;
-  // The CTA's first row is loaded before the scale reduction so the two
-  // latencies overlap; every row after that streams with two vectors in flight
-  // per thread.
-  int t = blockIdx.x;
-  uint4 a = make_uint4(0, 0, 0, 0), b = make_uint4(0, 0, 0, 0);
-  if (t < p.T) {
-    const uint8_t* src = p.q + (int64_t)t * p.ldq;
-    if (tid < nch) a = ld_nc_v4(src + (int64_t)tid * 16);
-    if (tid + kThreads < nch) b = ld_nc_v4(src + (int64_t)(tid + kThreads) * 16);
+  // Each warp's first row is loaded before the scale reduction so the two
+  // latencies overlap.
+  int t = gwarp;
+  uint4 v[kPass];
+#pragma unroll
+  for (int j = 0; j < kPass; ++j) {
+    const int c = j * 32 + lane;
+    v[j] = (t < p.T && c < nch) ? ld_nc_v4(p.q + (int64_t)t * p.ldq + (int64_t)c * 16)
+                                : make_uint4(0, 0, 0, 0);
   }
   float S;
   if constexpr (MODE == kRequantAmax) {
@@ -137,29 +144,27 @@ __global__ void __launch_bounds__(kThreads) requant_kernel(RequantArgs p) {
   }
   if (blockIdx.x == 0 && tid == 0) *p.scale_out = (S > 0.0f) ? S : 1.0f;
 
-  for (; t < p.T; t += gridDim.x) {
+  bool preloaded = true;
+  for (; t < p.T; t += nwarps) {
     const float r = (S > 0.0f) ? __fdiv_rn(token_scale<SFMT>(p, t), S) : 0.0f;
     const uint8_t* src = p.q + (int64_t)t * p.ldq;
     uint8_t* dst = p.q_out + (int64_t)t * p.H;
-    for (int c = tid; c < nch; c += 2 * kThreads) {
-      const int c2 = c + kThreads;
-      if (c > tid) {  // passes after the first: load here (the first pass was preloaded)
-        a = ld_nc_v4(src + (int64_t)c * 16);
-        b = (c2 < nch) ? ld_nc_v4(src + (int64_t)c2 * 16) : make_uint4(0, 0, 0, 0);
+    for (int c0 = 0; c0 < nch; c0 += 32 * kPass) {
+      if (!preloaded) {
+#pragma unroll
+        for (int j = 0; j < kPass; ++j) {
+          const int c = c0 + j * 32 + lane;
+          v[j] = (c < nch) ? ld_nc_v4(src + (int64_t)c * 16) : make_uint4(0, 0, 0, 0);
+        }
       }
-      st_v4(dst + (int64_t)c * 16,
-            make_uint4(requant4(a.x, r), requant4(a.y, r), requant4(a.z, r), requant4(a.w, r)));
-      if (c2 < nch)
-        st_v4(dst + (int64_t)c2 * 16,
-              make_uint4(requant4(b.x, r), requant4(b.y, r), requant4(b.z, r), requant4(b.w, r)));
-    }
-    // preload the first pass of this CTA's next row
-    const int tn = t + gridDim.x;
-    if (tn < p.T) {
-      const uint8_t* nsrc = p.q + (int64_t)tn * p.ldq;
-      a = (tid < nch) ? ld_nc_v4(nsrc + (int64_t)tid * 16) : make_uint4(0, 0, 0, 0);
-      b = (tid + kThreads < nch) ? ld_nc_v4(nsrc + (int64_t)(tid + kThreads) * 16)
-                                 : make_uint4(0, 0, 0, 0);
+      preloaded = false;
+#pragma unroll
+      for (int j = 0; j < kPass; ++j) {
+        const int c = c0 + j * 32 + lane;
+        if (c < nch)
+          st_v4(dst + (int64_t)c * 16, make_uint4(requant4(v[j].x, r), requant4(v[j].y, r),
+                                                  requant4(v[j].z, r), requant4(v[j].w, r)));
+      }
     }
   }
 }
@@ -171,7 +176,8 @@ cudaError_t launch_rows(Kern k, const RequantArgs& a, int num_sms, cudaStream_t 
   if (err != cudaSuccess) return err;
   if (per_sm < 1) per_sm = 1;
   int64_t grid = (int64_t)num_sms * per_sm;
-  if (grid > a.T) grid = a.T;
+  const int64_t need = ((int64_t)a.T + kThreads / 32 - 1) / (kThreads / 32);  // one warp per row
+  if (grid > need) grid = need;
   if (grid < 1) grid = 1;
   k<<<(unsigned)grid, kThreads, 0, s>>>(a);
   return cudaGetLastError();

@@ -93,10 +93,15 @@ def lib():
 
 
 def _ptr(t):
+    """Device address of a CUDA tensor (or a raw integer address, or None).
+    A CPU tensor is rejected here: its host address would reach a kernel."""
     if t is None:
         return None
     if isinstance(t, int):
         return C.c_void_p(t)
+    if t.device.type != "cuda":
+        raise ValueError(f"moeperm: tensor on {t.device}, but every tensor argument must be on "
+                         "a CUDA device")
     return C.c_void_p(t.data_ptr())
 
 

@@ -121,3 +121,10 @@ def test_other_calls_reject(mp):
     assert mp.fp8_requant_per_tensor(FAKE, 7000, FAKE, 16, 7168, FAKE, FAKE, S) == E
     assert mp.moe_status_sync(None, S) == E
     assert "invalid" in mp.lib().moe_status_string(E).decode()
+
+
+def test_binding_rejects_cpu_tensors(mp):
+    import torch
+    x = torch.zeros(16, dtype=torch.uint8)
+    with pytest.raises(ValueError):
+        mp.moe_quant_group(x, 16, 1, None, 16, 32, "u8", FAKE, FAKE, 1, FAKE, _NullStream())

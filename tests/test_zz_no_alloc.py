@@ -48,7 +48,10 @@ def _args(x, ids, w, T, H, K, E, L, b, g, o, bound, ld):
 
 
 def test_noalloc_matches_workspace_dispatch_two_calls(dev):
-    T, H, K, E, L, b, g = 512, 1024, 8, 256, 256, 128, 128
+    # 5120 slots: above the 4096-slot one-launch path, so the two-launch path
+    # runs and its chunk table lives in the library's static scratch array
+    T, H, K, E, L, b, g = 640, 1024, 8, 256, 256, 128, 128
+    assert T * K > 4096
     assert dev.moe_workspace_bytes(T, K, L) <= 64 * 1024 + 256
     ws = dev.Workspace(T, K, L, DEV)
     for seed in (0, 1):
