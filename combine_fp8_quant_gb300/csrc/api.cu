@@ -46,7 +46,7 @@ bool ld_ok(int fmt, int64_t ld, int64_t rows_per_block, int G) {
 }
 
 int64_t route_nchunks(int64_t A, int S) {
-  const int64_t per = 256 * (int64_t)S;
+  const int64_t per = kRouteThreads * (int64_t)S;
   int64_t n = (A + per - 1) / per;
   return n < 1 ? 1 : n;
 }
@@ -102,7 +102,7 @@ moe_status_t run_dispatch(const DispatchCommon& c, int mode, int32_t block_e, in
   RoutePlanArgs rp{};
   rp.ids = c.ids; rp.d_num_tokens = c.d_num_tokens;
   rp.T = c.T; rp.K = c.K; rp.L = c.L;
-  rp.chunk = 256 * S; rp.nchunks = (int32_t)nchunks;
+  rp.chunk = kRouteThreads * S; rp.nchunks = (int32_t)nchunks;
   rp.lrank = c.src2dst; rp.table = table; rp.status = d_status;
   if (launch_route_plan(rp, S, stream) != cudaSuccess) return MOE_ERR_CUDA;
 

@@ -15,6 +15,11 @@ constexpr int kMaxTableInts = 16384;
 // ---------------------------------------------------------------------------
 // Route plan: per-chunk expert histograms and stable in-chunk ranks.
 // ---------------------------------------------------------------------------
+#ifndef MOEPERM_ROUTE_WARPS
+#define MOEPERM_ROUTE_WARPS 8
+#endif
+constexpr int kRouteWarps = MOEPERM_ROUTE_WARPS;
+constexpr int kRouteThreads = 32 * kRouteWarps;   // a chunk holds kRouteThreads * S slots
 struct RoutePlanArgs {
   const int32_t* ids;          // [T, K]
   const int32_t* d_num_tokens; // optional live tokens

@@ -50,6 +50,14 @@ namespace {
 #ifndef MOEPERM_SCATTER_CPT
 #define MOEPERM_SCATTER_CPT 2
 #endif
+// 1: payload rows leave through TMA bulk copies from a shared-memory staging
+// buffer; 0: each thread stores its 16-byte vectors to every destination row.
+#ifndef MOEPERM_SCATTER_TMA
+#define MOEPERM_SCATTER_TMA 1
+#endif
+#ifndef MOEPERM_SCATTER_MIN_BLOCKS
+#define MOEPERM_SCATTER_MIN_BLOCKS 1
+#endif
 constexpr int kCPT = MOEPERM_SCATTER_CPT;          // 16-element chunks per thread
 constexpr int kStages = MOEPERM_SCATTER_STAGES;    // staged rows in flight to the bulk-copy engine
 
@@ -208,7 +216,7 @@ __device__ void layout_prologue(const ScatterArgs& p, int32_t* tbl, int32_t* st,
 }
 
 template <int GSZ, int FMT>
-__global__ void __launch_bounds__(1024) quant_scatter_kernel(ScatterArgs p) {
+__global__ void __launch_bounds__(1024, MOEPERM_SCATTER_MIN_BLOCKS) quant_scatter_kernel(ScatterArgs p) {
   extern __shared__ int32_t sm[];
   __shared__ int32_t s_wsum[32];
   const int tid = threadIdx.x, lane = tid & 31, bd = blockDim.x;
@@ -321,20 +329,32 @@ __global__ void __launch_bounds__(1024) quant_scatter_kernel(ScatterArgs p) {
         q0 = quant8(v[i][0], inv);
         q1 = quant8(v[i][1], inv);
       }
-      if (active) *reinterpret_cast<uint4*>(sb + c * 16) = make_uint4(q0.x, q0.y, q1.x, q1.y);
+      if (active) {
+        const uint4 qv = make_uint4(q0.x, q0.y, q1.x, q1.y);
+        if constexpr (MOEPERM_SCATTER_TMA) {
+          *reinterpret_cast<uint4*>(sb + c * 16) = qv;
+        } else {
+          for (int k = 0; k < nslots; ++k) {
+            const int row = rows[k];
+            if (row >= 0) st_v4(p.xq + (int64_t)row * H + c * 16, qv);
+          }
+        }
+      }
       const int cw = i * bd + (tid & ~31);  // first chunk of this warp
       if (cw < nch)
         store_scales<GSZ, FMT>(p, nslots, rows, lane, active, e, sval, cw * 16 / GSZ, G, G4);
     }
-    fence_proxy_async_smem();
-    if (tid == 0) bulk_wait_read<kStages - 2>();
-    __syncthreads();
-    if (tid == 0) {
-      for (int k = 0; k < nslots; ++k) {
-        const int row = rows[k];
-        if (row >= 0) bulk_store_s2g(p.xq + (int64_t)row * H, stage_s + (uint32_t)(buf * H), (uint32_t)H);
+    if constexpr (MOEPERM_SCATTER_TMA) {
+      fence_proxy_async_smem();
+      if (tid == 0) bulk_wait_read<kStages - 2>();
+      __syncthreads();
+      if (tid == 0) {
+        for (int k = 0; k < nslots; ++k) {
+          const int row = rows[k];
+          if (row >= 0) bulk_store_s2g(p.xq + (int64_t)row * H, stage_s + (uint32_t)(buf * H), (uint32_t)H);
+        }
+        bulk_commit();
       }
-      bulk_commit();
     }
 #pragma unroll
     for (int i = 0; i < kCPT; ++i) {
@@ -342,7 +362,9 @@ __global__ void __launch_bounds__(1024) quant_scatter_kernel(ScatterArgs p) {
       v[i][1] = vn[i][1];
     }
   }
-  if (tid == 0) bulk_wait_all();
+  if constexpr (MOEPERM_SCATTER_TMA) {
+    if (tid == 0) bulk_wait_all();
+  }
 }
 
 template <int GSZ, int FMT>
@@ -356,14 +378,14 @@ cudaError_t launch_one(const ScatterArgs& a, int num_sms, bool pdl, cudaStream_t
   int per_sm = 0;
   cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
       &per_sm, quant_scatter_kernel<GSZ, FMT>, bd,
-      stage_offset(a, 16) + (size_t)kStages * a.H);
+      stage_offset(a, 16) + (MOEPERM_SCATTER_TMA ? (size_t)kStages * a.H : 0));
   if (err != cudaSuccess) return err;
   if (per_sm < 1) per_sm = 1;
   int64_t grid = (int64_t)num_sms * per_sm;
   if (grid > a.T) grid = a.T;
   if (grid < 1) grid = 1;
   const int64_t ntok_max = (a.T + grid - 1) / grid;
-  const size_t smem = stage_offset(a, ntok_max) + (size_t)kStages * a.H;
+  const size_t smem = stage_offset(a, ntok_max) + (MOEPERM_SCATTER_TMA ? (size_t)kStages * a.H : 0);
   if (smem > 48 * 1024) {
     err = cudaFuncSetAttribute(quant_scatter_kernel<GSZ, FMT>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

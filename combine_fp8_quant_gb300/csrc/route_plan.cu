@@ -9,13 +9,13 @@
 // The prefix sums over chunks and experts (segment starts, psum, total,
 // masked_m) are formed from this table by every CTA of the scatter launch.
 //
-// Design (fixed grid of `nchunks` CTAs of 8 warps): CTA c owns slots
+// Design (fixed grid of `nchunks` CTAs of kRouteWarps warps): CTA c owns slots
 // [c*chunk, (c+1)*chunk); warp w owns a contiguous sub-range of 32*S of them,
 // walked in order in steps of 32. In a step, ballots over the bits of the
 // expert id group the lanes with the same expert; a lane's rank among them is
 // the popcount of its lower peers, and the lowest peer adds the group size to
-// the warp's per-expert counter in shared memory. A per-expert scan over the 8 warps turns the
-// warp-local ranks into chunk-local ones. Deterministic and stable, with no
+// the warp's per-expert counter in shared memory. A per-expert scan over the
+// warps turns the warp-local ranks into chunk-local ones. Deterministic and stable, with no
 // global atomics. The CTA signals the dependent scatter launch at its start,
 // so that launch is scheduled while this one runs (it waits for this grid's
 // results before reading them).
@@ -26,8 +26,8 @@ namespace moeperm {
 
 namespace {
 
-constexpr int kWarps = 8;
-constexpr int kThreads = kWarps * 32;
+constexpr int kWarps = kRouteWarps;
+constexpr int kThreads = kRouteThreads;
 constexpr int kGroup = 8;  // steps whose peer masks are formed together
 #ifndef MOEPERM_ROUTE_MAX_CHUNKS
 #define MOEPERM_ROUTE_MAX_CHUNKS 16

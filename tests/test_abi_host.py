@@ -128,3 +128,11 @@ def test_binding_rejects_cpu_tensors(mp):
     x = torch.zeros(16, dtype=torch.uint8)
     with pytest.raises(ValueError):
         mp.moe_quant_group(x, 16, 1, None, 16, 32, "u8", FAKE, FAKE, 1, FAKE, _NullStream())
+
+
+def test_size_limits_rejected(mp):
+    assert call_compact(mp, H=32768 + 128, ldx=32768 + 128) == mp.MOE_ERR_INVALID_ARG
+    assert call_compact(mp, T=(1 << 20) // 8 + 1) == mp.MOE_ERR_INVALID_ARG
+    # chunk table beyond 64 KiB: 1024 experts with 2^19 slots
+    assert mp.moe_workspace_bytes(65536, 8, 1024) == 0
+    assert call_compact(mp, T=65536, L=1024, E=1024, workspace_bytes=1 << 24) == mp.MOE_ERR_INVALID_ARG

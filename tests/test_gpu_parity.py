@@ -722,3 +722,57 @@ def test_prefill_full_size_sampled(dev, ref):
                                np.ascontiguousarray(w[t:t + 1]), 1, K, H)
         got = o[t].view(torch.int16).cpu().numpy().view(np.uint16)
         assert np.array_equal(got, want[0])
+
+
+# ---------------------------------------------------------------------------
+# Maximum sizes
+# ---------------------------------------------------------------------------
+
+def test_dispatch_max_assignments(dev, ref):
+    """T*K = 2^20 slots (the largest accepted): 256 route-plan chunks of 4096
+    slots x 64 experts, a full 64 KiB chunk table."""
+    rng = np.random.default_rng(20)
+    T, K, L, H = 131072, 8, 64, 128
+    x = synth.normal_bf16(rng, (T, H))
+    ids = rng.integers(-1, L + 2, size=(T, K)).astype(np.int32)   # a few dropped slots
+    w = rng.random((T, K)).astype(np.float32)
+    assert dev.moe_workspace_bytes(T, K, L) == 256 + 16384 * 4
+    compact_both(dev, ref, x, ids, w, H, K, L + 2, L, 128, 128, "packed", with_rw=False)
+
+
+@pytest.mark.parametrize("T", [9, 1100])     # 18 slots: one launch; 2200: two launches
+def test_dispatch_max_hidden(dev, ref, T):
+    """H = 32768: the two-launch scatter covers the row with 1024 threads x 2
+    chunks of 16 in one pass; the one-launch path loops four passes."""
+    rng = np.random.default_rng(21)
+    K, L, H = 2, 8, 32768
+    x = synth.normal_bf16(rng, (T, H), outlier_frac=0.01)
+    ids = synth.uniform_topk(rng, T, L, K)
+    w = synth.softmax_weights(rng, T, K)
+    compact_both(dev, ref, x, ids, w, H, K, L, L, 128, 128, "packed")
+    masked_both(dev, ref, x, ids, w, H, K, 16, L, 8, 128, "u8")
+
+
+@pytest.mark.parametrize("T", [64, 100])     # 2048 slots: one launch; 3200: two launches
+def test_dispatch_max_topk_and_experts(dev, ref, T):
+    """K = 32 slots per token over L = 1024 local experts."""
+    rng = np.random.default_rng(22 + T)
+    K, L, H = 32, 1024, 256
+    x = synth.normal_bf16(rng, (T, H))
+    ids = synth.uniform_topk(rng, T, L, K)
+    w = synth.softmax_weights(rng, T, K)
+    compact_both(dev, ref, x, ids, w, H, K, L, L, 128, 128, "u8")
+    y = synth.normal_bf16(rng, (dev.moe_compact_bound(T * K, L, 128), H))
+    r, _, _ = compact_both(dev, ref, x, ids, w, H, K, L, L, 128, 128, "packed")
+    check_combine(dev, ref, y, r["s2d"], w, H)
+
+
+def test_dispatch_max_experts_two_launch(dev, ref):
+    """L = 1024 with 160000 slots: 10 chunks x 1024 experts, within the 64 KiB table."""
+    rng = np.random.default_rng(23)
+    T, K, L, H = 20000, 8, 1024, 128
+    x = synth.normal_bf16(rng, (T, H))
+    ids = synth.zipf_topk(rng, T, L, K, n_empty=40)
+    w = synth.softmax_weights(rng, T, K)
+    compact_both(dev, ref, x, ids, w, H, K, L, L, 128, 128, "packed", with_rw=False)
+    masked_both(dev, ref, x, ids, w, H, K, L, L, 512, 128, "packed")
