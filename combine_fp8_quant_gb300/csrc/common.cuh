@@ -185,9 +185,28 @@ __device__ __forceinline__ void bulk_wait_read() {
 __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
+// Asynchronous 16-byte copy global -> shared (both addresses 16-byte
+// aligned), completed by cp_async_wait_all() in the issuing thread.
+__device__ __forceinline__ void cp_async16(void* sdst, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+               ::"r"((uint32_t)__cvta_generic_to_shared(sdst)), "l"(gsrc)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
 // Make this thread's generic-proxy shared-memory writes visible to bulk copies.
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Lets a kernel take `dyn` bytes of dynamic shared memory. Without the
+// opt-in a CTA is limited to 48 KiB of dynamic plus static shared memory; the
+// static arrays of these kernels stay under 1 KiB.
+template <typename Kern>
+inline cudaError_t opt_in_smem(Kern kernel, size_t dyn) {
+  if (dyn + 1024 <= 48 * 1024) return cudaSuccess;
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
 }
 
 __device__ __forceinline__ int64_t align_up64(int64_t c, int64_t b) { return (c + b - 1) / b * b; }

@@ -303,13 +303,10 @@ __global__ void __launch_bounds__(kThreads) dispatch_small_kernel(ScatterArgs p)
 template <int GSZ, int FMT, int S>
 cudaError_t launch_s(const ScatterArgs& a, int num_sms, cudaStream_t s) {
   const size_t smem = ((size_t)kWarps * a.L + 2 * (size_t)a.L + (size_t)a.T * a.K) * sizeof(int32_t);
-  if (smem > 48 * 1024) {
-    cudaError_t err = cudaFuncSetAttribute(dispatch_small_kernel<GSZ, FMT, S>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
-  }
+  cudaError_t err = opt_in_smem(dispatch_small_kernel<GSZ, FMT, S>, smem);
+  if (err != cudaSuccess) return err;
   int per_sm = 0;
-  cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
       &per_sm, dispatch_small_kernel<GSZ, FMT, S>, kThreads, smem);
   if (err != cudaSuccess) return err;
   if (per_sm < 1) per_sm = 1;

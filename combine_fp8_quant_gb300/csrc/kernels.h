@@ -62,6 +62,7 @@ struct ScatterArgs {
   int32_t* total;              // [1]
   int32_t* masked_m;           // masked output [L]
   int32_t* status;
+  int32_t stages, pre;         // scatter: staging ring size, tokens staged before the wait
 };
 cudaError_t launch_quant_scatter(const ScatterArgs& a, int g, int fmt, int num_sms,
                                  bool after_route_plan, cudaStream_t s);

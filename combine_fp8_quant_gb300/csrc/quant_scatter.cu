@@ -22,11 +22,15 @@
 // walks the live tokens, t = blockIdx.x + i * gridDim.x. One thread owns two
 // 16-element chunks of a row (two 16-byte loads each), so a single pass
 // covers H <= 32768.
-//   Prologue: the CTA issues its first token's loads, then waits for the route
-//   plan (programmatic dependent launch: this grid is already resident while
-//   the route plan runs), loads the chunk table (<= 64 KiB) into shared memory,
-//   scans it, and resolves the rows of all of its own slots at once. The
-//   route plan therefore needs no serial "last block" and no fence.
+//   Prologue: this grid is already resident while the route plan runs
+//   (programmatic dependent launch), so before waiting for it a CTA reads and
+//   quantises its first few tokens into their staging buffers (inputs only:
+//   their rows are not known yet) and loads the expert ids of its first slots
+//   (one per thread). After the wait it loads the chunk table (<= 64 KiB)
+//   into shared memory, scans it, and resolves the rows of all of its own
+//   slots at once. The route plan therefore needs no serial "last block" and
+//   no fence. The m_indices fill runs after the token loop, while the last
+//   bulk copies drain.
 //   Token loop: the next token's loads are issued before the current token is
 //   processed; the g/16 lanes of a group reduce the group max with xor
 //   shuffles on sign-cleared bf16 bit patterns; the exponent comes from the
@@ -45,31 +49,50 @@ namespace moeperm {
 namespace {
 
 #ifndef MOEPERM_SCATTER_STAGES
-#define MOEPERM_SCATTER_STAGES 3
+#define MOEPERM_SCATTER_STAGES 4
+#endif
+#ifndef MOEPERM_SCATTER_PRE
+#define MOEPERM_SCATTER_PRE 2
 #endif
 #ifndef MOEPERM_SCATTER_CPT
 #define MOEPERM_SCATTER_CPT 2
-#endif
-// 1: payload rows leave through TMA bulk copies from a shared-memory staging
-// buffer; 0: each thread stores its 16-byte vectors to every destination row.
-#ifndef MOEPERM_SCATTER_TMA
-#define MOEPERM_SCATTER_TMA 1
 #endif
 #ifndef MOEPERM_SCATTER_MIN_BLOCKS
 #define MOEPERM_SCATTER_MIN_BLOCKS 1
 #endif
 constexpr int kCPT = MOEPERM_SCATTER_CPT;          // 16-element chunks per thread
-constexpr int kStages = MOEPERM_SCATTER_STAGES;    // staged rows in flight to the bulk-copy engine
+// Largest staging ring (rows in flight to the bulk-copy engine) and number of
+// tokens quantised before the wait on the route plan; the launch lowers both
+// when shared memory is short (large H with a large chunk table).
+constexpr int kStages = MOEPERM_SCATTER_STAGES;
+constexpr int kPre = MOEPERM_SCATTER_PRE < kStages ? MOEPERM_SCATTER_PRE : kStages;
+static_assert(kStages >= 2 && kStages <= 6, "staging ring of 2 to 6 rows");
 
 // Dynamic shared memory: [table nchunks*L | starts L | psum L | rows ntok*K]
-// (dispatch modes only), then kStages staged rows of H bytes at a 128-byte
-// boundary.
+// (dispatch modes only), then, at a 128-byte boundary, p.stages staged rows of
+// H bytes and the scales of the tokens staged early (p.pre x kCPT x threads
+// words).
 __host__ __device__ inline size_t layout_bytes(const ScatterArgs& p, int64_t ntok) {
   if (p.mode == kModeIdentity) return 0;
   return ((size_t)p.nchunks * p.L + 2 * (size_t)p.L + (size_t)ntok * p.K) * sizeof(int32_t);
 }
 __host__ __device__ inline size_t stage_offset(const ScatterArgs& p, int64_t ntok) {
   return (layout_bytes(p, ntok) + 127) / 128 * 128;
+}
+__host__ __device__ inline size_t smem_bytes(const ScatterArgs& p, int64_t ntok, int bd) {
+  return stage_offset(p, ntok) + (size_t)p.stages * p.H + (size_t)p.pre * kCPT * bd * sizeof(int32_t);
+}
+
+// Wait until at most n - 2 bulk groups of this thread still read shared
+// memory (n = staging ring size, 2..6; the wait takes an immediate).
+__device__ __forceinline__ void wait_ring(int n) {
+  switch (n) {
+    case 2: bulk_wait_read<0>(); break;
+    case 3: bulk_wait_read<1>(); break;
+    case 4: bulk_wait_read<2>(); break;
+    case 5: bulk_wait_read<3>(); break;
+    default: bulk_wait_read<4>(); break;
+  }
 }
 // Tokens per CTA the row buffer is sized for (ceil(T / grid)).
 __device__ inline int64_t ntok_smem(const ScatterArgs& p) {
@@ -154,7 +177,12 @@ __device__ void layout_prologue(const ScatterArgs& p, int32_t* tbl, int32_t* st,
                                 int32_t* s_wsum) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, bd = blockDim.x;
   const int L = p.L, NC = p.nchunks;
-  for (int i = tid; i < NC * L; i += bd) tbl[i] = __ldcg(p.table + i);
+  // the whole table in flight at once: 16-byte asynchronous copies (the
+  // table starts 16-byte aligned in the workspace), the odd tail by loads
+  const int n = NC * L, n4 = n / 4;
+  for (int i = tid; i < n4; i += bd) cp_async16(tbl + 4 * i, p.table + 4 * i);
+  for (int i = 4 * n4 + tid; i < n; i += bd) tbl[i] = __ldcg(p.table + i);
+  cp_async_wait_all();
   __syncthreads();
   for (int e = tid; e < L; e += bd) {
     int run = 0;
@@ -215,6 +243,56 @@ __device__ void layout_prologue(const ScatterArgs& p, int32_t* tbl, int32_t* st,
   }
 }
 
+// Quantises one thread's 16-element chunk (a, b) of a row: the group maximum
+// over the GSZ/16 lanes of the group (xor shuffles over sign-cleared bf16
+// bits), the group's exponent e (or plain fp32 scale sval) and the 16 e4m3
+// codes. Every lane of the warp must call it.
+template <int GSZ, int FMT>
+__device__ __forceinline__ uint4 quant_chunk(const uint4& a, const uint4& b, int& e, float& sval) {
+  uint32_t m = amax16_bf16(a, b);
+#pragma unroll
+  for (int off = 1; off < GSZ / 16; off <<= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
+  const float amax = __uint_as_float(m << 16);
+  uint2 q0, q1;
+  e = 0;
+  sval = 0.0f;
+  if constexpr (FMT == kFmtF32) {
+    sval = __fdiv_rn(fmaxf(amax, 1e-10f), 448.0f);
+    q0 = quant8_div(a, sval);
+    q1 = quant8_div(b, sval);
+  } else {
+    e = (FMT == kFmtMX) ? mx_exponent(amax) : group_exponent(amax);
+    const float inv = exp2_neg(e);
+    q0 = quant8(a, inv);
+    q1 = quant8(b, inv);
+  }
+  return make_uint4(q0.x, q0.y, q1.x, q1.y);
+}
+
+// Row of slot a (expert e, chunk-local rank lr) from the prologue's tables;
+// -1 if dropped. A rank that does not fit the layout (only possible if the
+// workspace was altered between the launches) flags BAD_LAYOUT and drops the
+// slot, so no write ever leaves the buffers.
+__device__ __forceinline__ int slot_row(const ScatterArgs& p, const int32_t* tbl, const int32_t* st,
+                                        int64_t a, int e, int lr) {
+  if (e < 0 || e >= p.L) return -1;
+  const int base = tbl[(int)(a / p.chunk) * p.L + e];
+  if (p.mode == kModeCompact) {
+    const int row = st[e] + base + lr;
+    if (lr < 0 || row < 0 || (int64_t)row >= p.bound) {
+      set_status(p.status, kStBadLayout);
+      return -1;
+    }
+    return row;
+  }
+  const int j = base + lr;
+  if (lr < 0 || j < 0) {
+    set_status(p.status, kStBadLayout);
+    return -1;
+  }
+  return j < p.cap ? e * p.cap + j : -1;
+}
+
 template <int GSZ, int FMT>
 __global__ void __launch_bounds__(1024, MOEPERM_SCATTER_MIN_BLOCKS) quant_scatter_kernel(ScatterArgs p) {
   extern __shared__ int32_t sm[];
@@ -228,55 +306,75 @@ __global__ void __launch_bounds__(1024, MOEPERM_SCATTER_MIN_BLOCKS) quant_scatte
   const int nslots = identity ? 1 : p.K;
   const int n_live = live_count(p.d_num_tokens, p.T, p.status,
                                 identity && blockIdx.x == 0 && tid == 0);
-
-  // first token's loads go out before anything waits
-  uint4 v[kCPT][2];
-  load_row(v, (int)blockIdx.x < n_live ? p.x + (int64_t)blockIdx.x * p.ldx : nullptr, nch, bd, tid);
-
   const int ntok =
       n_live > (int)blockIdx.x ? (n_live - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-  int32_t* rows_s = sm;  // identity mode: unused
-  if (!identity) {
-    pdl_wait_primary();
-    const int L = p.L;
-    int32_t* tbl = sm;
-    int32_t* st = tbl + p.nchunks * L;
-    int32_t* ps = st + L;
-    rows_s = ps + L;
-    layout_prologue(p, tbl, st, ps, s_wsum);
+  const int nsl = identity ? 0 : ntok * p.K;  // slots of this CTA: i -> token i / K, slot i % K
+  auto slot_of = [&](int i) -> int64_t {
+    return (int64_t)(blockIdx.x + (i / p.K) * gridDim.x) * p.K + (i % p.K);
+  };
 
-    if (p.mode == kModeCompact && p.m_indices != nullptr) {
-      for (int64_t r = (int64_t)blockIdx.x * bd + tid; r < p.bound; r += (int64_t)gridDim.x * bd) {
-        int lo = 0, hi = L - 1;  // largest e with start[e] <= r (start[0] = 0)
-        while (lo < hi) {
-          const int mid = (lo + hi + 1) >> 1;
-          if (st[mid] <= r) lo = mid; else hi = mid - 1;
-        }
-        p.m_indices[r] = (r < ps[lo]) ? lo : -1;
+  // Inputs only, before anything waits: the first token's row and the expert
+  // id of this thread's first slot.
+  uint4 v[kCPT][2];
+  load_row(v, ntok > 0 ? p.x + (int64_t)blockIdx.x * p.ldx : nullptr, nch, bd, tid);
+  const int64_t a0 = tid < nsl ? slot_of(tid) : -1;
+  const int e0 = a0 >= 0 ? __ldg(p.ids + a0) : -1;
+
+  uint8_t* stage = reinterpret_cast<uint8_t*>(sm) + stage_offset(p, ntok_smem(p));
+  int32_t* pre_s = reinterpret_cast<int32_t*>(stage + (size_t)p.stages * H);  // [pre][kCPT][bd]
+  int32_t* rows_s = sm;  // identity mode: unused
+  int32_t* st = sm;
+  int32_t* ps = sm;
+  int npre = 0;
+  if (!identity) {
+    // The first p.pre tokens are quantised into their staging buffers while the
+    // route plan still runs (their rows are not known yet); their scales wait
+    // in shared memory.
+    npre = ntok < p.pre ? ntok : p.pre;
+    for (int j = 0; j < npre; ++j) {
+      uint4 vn[kCPT][2];
+      load_row(vn, j + 1 < ntok ? p.x + (int64_t)(blockIdx.x + (j + 1) * gridDim.x) * p.ldx : nullptr,
+               nch, bd, tid);
+      uint8_t* sb = stage + (size_t)j * H;
+#pragma unroll
+      for (int i = 0; i < kCPT; ++i) {
+        const int c = i * bd + tid;
+        int e;
+        float sval;
+        const uint4 qv = quant_chunk<GSZ, FMT>(v[i][0], v[i][1], e, sval);
+        if (c < nch) *reinterpret_cast<uint4*>(sb + c * 16) = qv;
+        pre_s[(j * kCPT + i) * bd + tid] = (FMT == kFmtF32) ? __float_as_int(sval) : e;
+      }
+#pragma unroll
+      for (int i = 0; i < kCPT; ++i) {
+        v[i][0] = vn[i][0];
+        v[i][1] = vn[i][1];
       }
     }
 
+    pdl_wait_primary();
+    const int lr0 = a0 >= 0 ? __ldcg(p.src2dst + a0) : -1;  // in flight with the table loads
+    const int L = p.L;
+    int32_t* tbl = sm;
+    st = tbl + p.nchunks * L;
+    ps = st + L;
+    rows_s = ps + L;
+    layout_prologue(p, tbl, st, ps, s_wsum);
+
     // rows of every slot this CTA will scatter
-    for (int i = tid; i < ntok * p.K; i += bd) {
-      const int t = blockIdx.x + (i / p.K) * gridDim.x;
-      const int64_t a = (int64_t)t * p.K + (i % p.K);
-      const int e = __ldg(p.ids + a);
-      int row = -1;
-      if (e >= 0 && e < L) {
-        const int lr = p.src2dst[a];
-        const int base = tbl[(int)(a / p.chunk) * L + e];
-        if (p.mode == kModeCompact) {
-          row = st[e] + base + lr;
-          if (lr < 0 || row < 0 || (int64_t)row >= p.bound) {  // never write outside the buffer
-            set_status(p.status, kStBadLayout);
-            row = -1;
-          }
-        } else {
-          const int j = base + lr;
-          if (lr < 0 || j < 0) set_status(p.status, kStBadLayout);
-          else if (j < p.cap) row = e * p.cap + j;
-        }
+    for (int i = tid; i < nsl; i += bd) {
+      int64_t a;
+      int e, lr;
+      if (i == tid) {
+        a = a0;
+        e = e0;
+        lr = lr0;
+      } else {
+        a = slot_of(i);
+        e = __ldg(p.ids + a);
+        lr = __ldcg(p.src2dst + a);
       }
+      const int row = slot_row(p, tbl, st, a, e, lr);
       p.src2dst[a] = row;
       if (row >= 0 && p.row_weights != nullptr) p.row_weights[row] = __ldg(p.w + a);
       rows_s[i] = row;
@@ -285,20 +383,21 @@ __global__ void __launch_bounds__(1024, MOEPERM_SCATTER_MIN_BLOCKS) quant_scatte
   }
 
   // ---- token loop ---------------------------------------------------------
-  // The quantised row is staged in shared memory (kStages rotating buffers)
+  // The quantised row is staged in shared memory (p.stages rotating buffers)
   // and thread 0 writes it to every destination row with bulk copies, so the
   // payload stores leave the SM as a few large TMA transfers. One barrier per
   // token publishes the staged row; before it, thread 0 waits until the bulk
   // copies that last read the NEXT buffer are done, so after it every thread
-  // may overwrite that buffer.
-  uint8_t* stage = reinterpret_cast<uint8_t*>(sm) + stage_offset(p, ntok_smem(p));
+  // may overwrite that buffer. Tokens staged before the wait only have their
+  // scales stored here.
   const uint32_t stage_s = (uint32_t)__cvta_generic_to_shared(stage);
   int ident_row[1];
   for (int it = 0; it < ntok; ++it) {
     const int t = blockIdx.x + it * gridDim.x;
+    const bool staged = it < npre;
     uint4 vn[kCPT][2];
     const int tn = t + gridDim.x;
-    load_row(vn, tn < n_live ? p.x + (int64_t)tn * p.ldx : nullptr, nch, bd, tid);
+    if (!staged) load_row(vn, tn < n_live ? p.x + (int64_t)tn * p.ldx : nullptr, nch, bd, tid);
     const int* rows;
     if (identity) {
       ident_row[0] = t;
@@ -306,91 +405,101 @@ __global__ void __launch_bounds__(1024, MOEPERM_SCATTER_MIN_BLOCKS) quant_scatte
     } else {
       rows = rows_s + it * p.K;
     }
-    const int buf = it % kStages;
+    const int buf = it % p.stages;
     uint8_t* sb = stage + (size_t)buf * H;
 #pragma unroll
     for (int i = 0; i < kCPT; ++i) {
       const int c = i * bd + tid;
       const bool active = c < nch;
-      uint32_t m = amax16_bf16(v[i][0], v[i][1]);
-#pragma unroll
-      for (int off = 1; off < GSZ / 16; off <<= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
-      const float amax = __uint_as_float(m << 16);
-      int e = 0;
-      float sval = 0.0f;
-      uint2 q0, q1;
-      if constexpr (FMT == kFmtF32) {
-        sval = __fdiv_rn(fmaxf(amax, 1e-10f), 448.0f);
-        q0 = quant8_div(v[i][0], sval);
-        q1 = quant8_div(v[i][1], sval);
+      int e;
+      float sval;
+      if (staged) {
+        const int w = pre_s[(it * kCPT + i) * bd + tid];
+        e = w;
+        sval = __int_as_float(w);
       } else {
-        e = (FMT == kFmtMX) ? mx_exponent(amax) : group_exponent(amax);
-        const float inv = exp2_neg(e);
-        q0 = quant8(v[i][0], inv);
-        q1 = quant8(v[i][1], inv);
-      }
-      if (active) {
-        const uint4 qv = make_uint4(q0.x, q0.y, q1.x, q1.y);
-        if constexpr (MOEPERM_SCATTER_TMA) {
-          *reinterpret_cast<uint4*>(sb + c * 16) = qv;
-        } else {
-          for (int k = 0; k < nslots; ++k) {
-            const int row = rows[k];
-            if (row >= 0) st_v4(p.xq + (int64_t)row * H + c * 16, qv);
-          }
-        }
+        const uint4 qv = quant_chunk<GSZ, FMT>(v[i][0], v[i][1], e, sval);
+        if (active) *reinterpret_cast<uint4*>(sb + c * 16) = qv;
       }
       const int cw = i * bd + (tid & ~31);  // first chunk of this warp
       if (cw < nch)
         store_scales<GSZ, FMT>(p, nslots, rows, lane, active, e, sval, cw * 16 / GSZ, G, G4);
     }
-    if constexpr (MOEPERM_SCATTER_TMA) {
-      fence_proxy_async_smem();
-      if (tid == 0) bulk_wait_read<kStages - 2>();
-      __syncthreads();
-      if (tid == 0) {
-        for (int k = 0; k < nslots; ++k) {
-          const int row = rows[k];
-          if (row >= 0) bulk_store_s2g(p.xq + (int64_t)row * H, stage_s + (uint32_t)(buf * H), (uint32_t)H);
-        }
-        bulk_commit();
+    fence_proxy_async_smem();
+    if (tid == 0) wait_ring(p.stages);
+    __syncthreads();
+    if (tid == 0) {
+      for (int k = 0; k < nslots; ++k) {
+        const int row = rows[k];
+        if (row >= 0) bulk_store_s2g(p.xq + (int64_t)row * H, stage_s + (uint32_t)(buf * H), (uint32_t)H);
+      }
+      bulk_commit();
+    }
+    if (!staged) {
+#pragma unroll
+      for (int i = 0; i < kCPT; ++i) {
+        v[i][0] = vn[i][0];
+        v[i][1] = vn[i][1];
       }
     }
-#pragma unroll
-    for (int i = 0; i < kCPT; ++i) {
-      v[i][0] = vn[i][0];
-      v[i][1] = vn[i][1];
+  }
+
+  // compact: m_indices over the whole static bound, while the last bulk
+  // copies drain
+  if (p.mode == kModeCompact && p.m_indices != nullptr) {
+    const int L = p.L;
+    for (int64_t r = (int64_t)blockIdx.x * bd + tid; r < p.bound; r += (int64_t)gridDim.x * bd) {
+      int lo = 0, hi = L - 1;  // largest e with start[e] <= r (start[0] = 0)
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (st[mid] <= r) lo = mid; else hi = mid - 1;
+      }
+      p.m_indices[r] = (r < ps[lo]) ? lo : -1;
     }
   }
-  if constexpr (MOEPERM_SCATTER_TMA) {
-    if (tid == 0) bulk_wait_all();
-  }
+  if (tid == 0) bulk_wait_all();
 }
 
 template <int GSZ, int FMT>
-cudaError_t launch_one(const ScatterArgs& a, int num_sms, bool pdl, cudaStream_t s) {
-  const int nch = a.H / 16;
+cudaError_t launch_one(const ScatterArgs& a0, int num_sms, bool pdl, cudaStream_t s) {
+  const int nch = a0.H / 16;
   int bd = (nch + kCPT - 1) / kCPT;
   bd = (bd + 31) / 32 * 32;
   if (bd > 1024) return cudaErrorInvalidValue;  // H > 32768 is rejected on the host
+  int dev = 0, optin = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err == cudaSuccess) err = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (err != cudaSuccess) return err;
+  const size_t budget = (size_t)optin - 1024;  // room for the static arrays
   // Resident CTAs per SM with a provisional row buffer of 16 tokens per CTA;
   // the grid is then fixed and the row buffer sized for ceil(T / grid) tokens.
+  // The staging ring and the early tokens shrink (down to two buffers and
+  // none) until one CTA fits the shared-memory budget.
+  ScatterArgs a = a0;
+  auto fit = [&](int64_t ntok) {
+    a.stages = kStages;
+    a.pre = (a.mode == kModeIdentity) ? 0 : kPre;
+    while (smem_bytes(a, ntok, bd) > budget && (a.pre > 0 || a.stages > 2)) {
+      if (a.pre > 0) --a.pre; else --a.stages;
+    }
+    if (a.pre > a.stages) a.pre = a.stages;
+  };
+  fit(16);
   int per_sm = 0;
-  cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      &per_sm, quant_scatter_kernel<GSZ, FMT>, bd,
-      stage_offset(a, 16) + (MOEPERM_SCATTER_TMA ? (size_t)kStages * a.H : 0));
+  err = opt_in_smem(quant_scatter_kernel<GSZ, FMT>, smem_bytes(a, 16, bd));
+  if (err != cudaSuccess) return err;
+  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quant_scatter_kernel<GSZ, FMT>, bd,
+                                                      smem_bytes(a, 16, bd));
   if (err != cudaSuccess) return err;
   if (per_sm < 1) per_sm = 1;
   int64_t grid = (int64_t)num_sms * per_sm;
   if (grid > a.T) grid = a.T;
   if (grid < 1) grid = 1;
   const int64_t ntok_max = (a.T + grid - 1) / grid;
-  const size_t smem = stage_offset(a, ntok_max) + (MOEPERM_SCATTER_TMA ? (size_t)kStages * a.H : 0);
-  if (smem > 48 * 1024) {
-    err = cudaFuncSetAttribute(quant_scatter_kernel<GSZ, FMT>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
-  }
+  fit(ntok_max);
+  const size_t smem = smem_bytes(a, ntok_max, bd);
+  err = opt_in_smem(quant_scatter_kernel<GSZ, FMT>, smem);
+  if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(bd);
