@@ -432,7 +432,11 @@ def load_traffic(which):
     return None
 
 
-def time_call(fn, flush, reps=20):
+def time_call(fn, flush, reps=40):
+    """Device time of one call in us, L2 flushed before each: the mean of
+    `reps` CUDA-event intervals with the top and bottom 10% dropped. Events on
+    this GPU tick in steps of about 2 us, so a median would snap to a tick;
+    the trimmed mean averages over the quantisation."""
     import torch
     for _ in range(3):
         fn()
@@ -446,13 +450,16 @@ def time_call(fn, flush, reps=20):
         b.record()
         torch.cuda.synchronize()
         ts.append(a.elapsed_time(b))
-    return statistics.median(ts) * 1e3  # us
+    ts.sort()
+    cut = reps // 10
+    kept = ts[cut:reps - cut]
+    return sum(kept) / len(kept) * 1e3  # us
 
 
 def other_rows(mp, dev, flush):
     """Decode (masked) dispatch + slab->expand + combine, MXFP8 live-row quant,
-    requant and expand->slab, each on its own workload (median of 20, L2
-    flushed before each call)."""
+    requant and expand->slab, each on its own workload (trimmed mean of 40,
+    L2 flushed before each call)."""
     import torch
     hbm, _ = peaks()
     res = {}
@@ -506,48 +513,55 @@ def other_rows(mp, dev, flush):
     res["mxfp8_live_quant"] = entry(us, cm["n_live"] * cm["H"] * 3 + cm["n_live"] * 224)
     res["mxfp8_live_quant"]["capacity_rows"] = cm["T_cap"]
 
-    # requant
+    # requant and expand <-> slab on the 4096-row workload, and on the same
+    # rows tiled 4x (16384 rows, 4x the expert blocks): the small workload is
+    # dominated by launch and first-access latency, the larger one shows the
+    # kernels' streaming rate.
     dr = synth.requant(0)
     cr = dr["cfg"]
-    q = torch.from_numpy(dr["q"]).to(dev)
-    s = torch.from_numpy(dr["s_tok"]).to(dev)
-    qo = torch.empty_like(q)
-    S = torch.empty(1, dtype=torch.float32, device=dev)
+    for tag, rep in (("", 1), ("_x4", 4)):
+        q = torch.from_numpy(np.tile(dr["q"], (rep, 1))).to(dev)
+        s = torch.from_numpy(np.tile(dr["s_tok"], rep)).to(dev)
+        T, H = q.shape
+        qo = torch.empty_like(q)
+        S = torch.empty(1, dtype=torch.float32, device=dev)
 
-    def rq():
-        assert mp.fp8_requant_per_tensor(q, cr["H"], s, cr["T"], cr["H"], qo, S) == 0
-    us = time_call(rq, flush)
-    res["requant_per_tensor"] = entry(us, 2 * cr["T"] * cr["H"] + cr["T"] * 4 + 4)
+        def rq():
+            assert mp.fp8_requant_per_tensor(q, H, s, T, H, qo, S) == 0
+        res["requant_per_tensor" + tag] = entry(time_call(rq, flush), 2 * T * H + T * 4 + 4)
+        res["requant_per_tensor" + tag]["rows"] = T
 
-    # expand -> slab -> expand (fp8 + packed scales), 64 experts, 4096 rows
-    counts = synth.repack_counts(dr["rng"], cr["L"], cr["blocks"], cr["align"])
-    psum_l, prev = [], 0
-    for cnt in counts:
-        st0 = -(-prev // 128) * 128
-        psum_l.append(st0 + int(cnt))
-        prev = st0 + int(cnt)
-    R = cr["T"]
-    capr = int(-(-counts.max() // 128) * 128)
-    psum = torch.tensor(psum_l, dtype=torch.int32, device=dev)
-    G = cr["H"] // 128
-    esc, ld_es = mp.scale_tensor("packed", R, cr["H"], 128, dev)
-    slab = torch.empty((cr["L"] * capr, cr["H"]), dtype=torch.uint8, device=dev)
-    ssc, ld_ss = mp.scale_tensor("packed", cr["L"] * capr, cr["H"], 128, dev, blocks=cr["L"])
-    mmr = torch.empty(cr["L"], dtype=torch.int32, device=dev)
-    back = torch.empty_like(q)
-    mi = torch.empty(R, dtype=torch.int32, device=dev)
-    real = int(counts.sum())
+        counts = synth.repack_counts(np.random.default_rng(17 + rep), cr["L"], cr["blocks"] * rep,
+                                     cr["align"])
+        psum_l, prev = [], 0
+        for cnt in counts:
+            st0 = -(-prev // 128) * 128
+            psum_l.append(st0 + int(cnt))
+            prev = st0 + int(cnt)
+        R = T
+        capr = int(-(-counts.max() // 128) * 128)
+        psum = torch.tensor(psum_l, dtype=torch.int32, device=dev)
+        G = H // 128
+        esc, ld_es = mp.scale_tensor("packed", R, H, 128, dev)
+        slab = torch.empty((cr["L"] * capr, H), dtype=torch.uint8, device=dev)
+        ssc, ld_ss = mp.scale_tensor("packed", cr["L"] * capr, H, 128, dev, blocks=cr["L"])
+        mmr = torch.empty(cr["L"], dtype=torch.int32, device=dev)
+        back = torch.empty_like(q)
+        mi = torch.empty(R, dtype=torch.int32, device=dev)
+        real = int(counts.sum())
 
-    def to_slab():
-        assert mp.moe_expand_to_slab(q, 1, cr["H"], R, esc, ld_es, psum, cr["L"], 128, capr, "packed",
-                                     128, slab, ssc, ld_ss, mmr, st) == 0
+        def to_slab():
+            assert mp.moe_expand_to_slab(q, 1, H, R, esc, ld_es, psum, cr["L"], 128, capr, "packed",
+                                         128, slab, ssc, ld_ss, mmr, st) == 0
 
-    def from_slab():
-        assert mp.moe_expand_from_slab(slab, 1, cr["H"], ssc, ld_ss, psum, cr["L"], 128, capr,
-                                       "packed", 128, None, back, R, esc, ld_es, mi, st) == 0
-    nb = 2 * real * (cr["H"] + ((G + 3) // 4) * 4) + cr["L"] * 8
-    res["expand_to_slab"] = entry(time_call(to_slab, flush), nb)
-    res["slab_to_expand"] = entry(time_call(from_slab, flush), nb + R * 4)
+        def from_slab():
+            assert mp.moe_expand_from_slab(slab, 1, H, ssc, ld_ss, psum, cr["L"], 128, capr,
+                                           "packed", 128, None, back, R, esc, ld_es, mi, st) == 0
+        nb = 2 * real * (H + ((G + 3) // 4) * 4) + cr["L"] * 8
+        res["expand_to_slab" + tag] = entry(time_call(to_slab, flush), nb)
+        res["slab_to_expand" + tag] = entry(time_call(from_slab, flush), nb + R * 4)
+        res["expand_to_slab" + tag]["real_rows"] = real
+        del q, qo, slab, back
     torch.cuda.synchronize()
     assert mp.moe_status_sync(st) == 0
     return res

@@ -185,8 +185,18 @@ __device__ void layout_prologue(const ScatterArgs& p, int32_t* tbl, int32_t* st,
   cp_async_wait_all();
   __syncthreads();
   for (int e = tid; e < L; e += bd) {
-    int run = 0;
-    for (int c = 0; c < NC; ++c) {
+    int run = 0, c = 0;
+    for (; c + 8 <= NC; c += 8) {  // 8 loads in flight, then 8 stores
+      int h[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) h[j] = tbl[(c + j) * L + e];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        tbl[(c + j) * L + e] = run;
+        run += h[j];
+      }
+    }
+    for (; c < NC; ++c) {
       const int h = tbl[c * L + e];
       tbl[c * L + e] = run;
       run += h;

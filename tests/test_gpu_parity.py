@@ -527,6 +527,23 @@ def test_repack_weighted_bf16(dev, ref):
     repack_both(dev, ref, exp, 2, H, psum, L, align, cap, weights=wts)
 
 
+@pytest.mark.parametrize("eb,H,weighted", [(2, 7184, True), (1, 7184, False), (2, 7168, False)])
+def test_repack_multi_segment_rows(dev, ref, eb, H, weighted):
+    """Rows longer than one 3.5 KB copy segment, with a ragged last segment
+    (H = 7184: 449 or 898 chunks of 16 bytes)."""
+    rng = np.random.default_rng(H + eb)
+    counts = [3, 0, 140, 1, 30]
+    align, cap, L = 128, 256, len(counts)
+    psum, starts, R = build_layout(counts, align)
+    if eb == 2:
+        exp = synth.normal_bf16(rng, (R, H)).view(np.uint8).reshape(R, 2 * H)
+    else:
+        exp = rng.integers(0, 256, size=(R, H), dtype=np.uint8)
+        exp[(exp & 0x7F) == 0x7F] = 0x11          # no NaN codes
+    wts = rng.random(R).astype(np.float32) if weighted else None
+    repack_both(dev, ref, exp, eb, H, psum, L, align, cap, weights=wts)
+
+
 def test_repack_bad_layout_flagged(dev, ref):
     H, L, align, cap = 16, 3, 4, 8
     exp = np.zeros((12, H), np.uint8)
@@ -561,8 +578,10 @@ def test_requant_config_full(dev, ref):
     requant_both(dev, ref, d["q"], d["s_tok"])
 
 
-@pytest.mark.parametrize("T,H", [(1, 16), (37, 1040), (300, 7168)])
+@pytest.mark.parametrize("T,H", [(1, 16), (37, 1040), (300, 7168), (5, 7184), (33, 3600), (3, 32768)])
 def test_requant_shapes(dev, ref, T, H):
+    """Rows of one, several and a ragged last segment of the conversion
+    launch's 3.5 KB segments."""
     d = synth.requant(T, T=T, H=H)
     requant_both(dev, ref, d["q"], d["s_tok"])
 
