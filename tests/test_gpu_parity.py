@@ -672,6 +672,49 @@ def test_graph_capture_replay_new_routing(dev, ref):
     assert int(st.item()) == 0
 
 
+def test_graph_capture_scatter_above_48k_shared_memory(dev, ref):
+    """Capture of a two-launch dispatch whose scatter CTA needs more than the
+    default 48 KiB of shared memory (1024 experts: a 36 KiB chunk table), so
+    the launch opts in while the stream is being captured; replays with new
+    routing must match the oracle."""
+    T, H, K, E, L, b, g = 1100, 4096, 2, 1024, 1024, 128, 128
+    rng = np.random.default_rng(41)
+    x = bf16_dev(synth.normal_bf16(rng, (T, H)))
+    ids = to_dev(synth.uniform_topk(rng, T, E, K))
+    w = to_dev(synth.softmax_weights(rng, T, K))
+    ws = dev.Workspace(T, K, L, DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        out = dev.dispatch_compact(x, ids, w, E, L, block_e=b, group_size=g, scale_fmt="u8",
+                                   workspace=ws, status=st)
+    bound = dev.moe_compact_bound(T * K, L, b)
+    for seed in (5, 6):
+        r = np.random.default_rng(seed)
+        xn = synth.normal_bf16(r, (T, H))
+        idn = synth.uniform_topk(r, T, E, K)
+        wn = synth.softmax_weights(r, T, K)
+        x.copy_(bf16_dev(xn))
+        ids.copy_(to_dev(idn))
+        w.copy_(to_dev(wn))
+        graph.replay()
+        torch.cuda.synchronize()
+        rxq = np.zeros((bound, H), np.uint8)
+        rsc, ld = ref.scale_buffer("u8", bound, H // g)
+        rmi = np.zeros(bound, np.int32)
+        rs2d = np.zeros((T, K), np.int32)
+        rc, rs, rp = (np.zeros(L, np.int32) for _ in range(3))
+        rt = np.zeros(1, np.int32)
+        ref.dispatch_compact(xn, T, T, H, idn, wn, K, L, b, g, "u8", rxq, rsc, ld, rmi, bound, rs2d,
+                             rc, rs, rp, rt)
+        assert np.array_equal(out["src2dst"].cpu().numpy(), rs2d)
+        assert np.array_equal(out["m_indices"].cpu().numpy(), rmi)
+        rows = rs2d[rs2d >= 0]
+        assert np.array_equal(out["xq"].cpu().numpy()[rows], rxq[rows])
+        assert np.array_equal(out["scales"].cpu().numpy()[rows], rsc[rows])
+    assert int(st.item()) == 0
+
+
 # ---------------------------------------------------------------------------
 # Full size, in the benchmark's launch configuration (prefill workload)
 # ---------------------------------------------------------------------------
