@@ -35,7 +35,8 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kCPT = 2;
 
 template <int GSZ, int FMT>
-__device__ __forceinline__ void small_store_scales(const ScatterArgs& p, const int* rows, int nslots,
+__device__ __forceinline__ void small_store_scales(const ScatterArgs& p, const int* rows,
+                                                   const int* exps, int nslots,
                                                    int lane, bool active, int e, float sval,
                                                    int group_base, int G, int G4) {
   constexpr int GL = GSZ / 16;
@@ -56,7 +57,7 @@ __device__ __forceinline__ void small_store_scales(const ScatterArgs& p, const i
         if (row < 0) continue;
         int64_t pk = row;
         if (p.mode == kModeMasked) {
-          const int ex = row / p.cap;
+          const int ex = exps[k];  // masked: one scale block per expert
           pk = (int64_t)ex * G4 * p.ld_s + (row - ex * p.cap);
         }
         sc[pk + wofs] = word;
@@ -101,6 +102,7 @@ __global__ void __launch_bounds__(kThreads) dispatch_small_kernel(ScatterArgs p)
   int32_t* st = hw + kWarps * L;      // [L] expert row base (compact start, masked 0)
   int32_t* ps = st + L;               // [L] count, then compact psum
   int32_t* rows_all = ps + L;         // [T*K] row of every slot
+  int32_t* exps_all = rows_all + (int64_t)p.T * K;  // [T*K] expert of every slot
 
   const int n_live = live_count(p.d_num_tokens, p.T, p.status, blockIdx.x == 0 && tid == 0);
   const int64_t A = (int64_t)p.T * K, A_live = (int64_t)n_live * K;
@@ -236,6 +238,7 @@ __global__ void __launch_bounds__(kThreads) dispatch_small_kernel(ScatterArgs p)
       else if (j < p.cap) row = e * p.cap + j;
     }
     rows_all[a] = row;
+    exps_all[a] = pk ? (pk & 0x7FF) - 1 : -1;
   }
   __syncthreads();
 
@@ -251,6 +254,7 @@ __global__ void __launch_bounds__(kThreads) dispatch_small_kernel(ScatterArgs p)
   // 5. quantise + scatter this CTA's tokens
   for (int t = t0; t < n_live; t += gridDim.x) {
     const int* rows = rows_all + (int64_t)t * K;
+    const int* exps = exps_all + (int64_t)t * K;
     for (int c0 = 0; c0 < nch; c0 += kCPT * kThreads) {
       if (t != t0 || c0 > 0) {
 #pragma unroll
@@ -294,7 +298,7 @@ __global__ void __launch_bounds__(kThreads) dispatch_small_kernel(ScatterArgs p)
           }
         const int cw = c0 + i * kThreads + (tid & ~31);
         if (cw < nch)
-          small_store_scales<GSZ, FMT>(p, rows, K, lane, active, e, sval, cw * 16 / GSZ, G, G4);
+          small_store_scales<GSZ, FMT>(p, rows, exps, K, lane, active, e, sval, cw * 16 / GSZ, G, G4);
       }
     }
   }
@@ -302,7 +306,7 @@ __global__ void __launch_bounds__(kThreads) dispatch_small_kernel(ScatterArgs p)
 
 template <int GSZ, int FMT, int S>
 cudaError_t launch_s(const ScatterArgs& a, int num_sms, cudaStream_t s) {
-  const size_t smem = ((size_t)kWarps * a.L + 2 * (size_t)a.L + (size_t)a.T * a.K) * sizeof(int32_t);
+  const size_t smem = ((size_t)kWarps * a.L + 2 * (size_t)a.L + 2 * (size_t)a.T * a.K) * sizeof(int32_t);
   cudaError_t err = opt_in_smem(dispatch_small_kernel<GSZ, FMT, S>, smem);
   if (err != cudaSuccess) return err;
   int per_sm = 0;

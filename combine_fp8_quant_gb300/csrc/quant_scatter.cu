@@ -68,13 +68,14 @@ constexpr int kStages = MOEPERM_SCATTER_STAGES;
 constexpr int kPre = MOEPERM_SCATTER_PRE < kStages ? MOEPERM_SCATTER_PRE : kStages;
 static_assert(kStages >= 2 && kStages <= 6, "staging ring of 2 to 6 rows");
 
-// Dynamic shared memory: [table nchunks*L | starts L | psum L | rows ntok*K]
+// Dynamic shared memory: [table nchunks*L | starts L | psum L | rows ntok*K |
+// experts ntok*K]
 // (dispatch modes only), then, at a 128-byte boundary, p.stages staged rows of
 // H bytes and the scales of the tokens staged early (p.pre x kCPT x threads
 // words).
 __host__ __device__ inline size_t layout_bytes(const ScatterArgs& p, int64_t ntok) {
   if (p.mode == kModeIdentity) return 0;
-  return ((size_t)p.nchunks * p.L + 2 * (size_t)p.L + (size_t)ntok * p.K) * sizeof(int32_t);
+  return ((size_t)p.nchunks * p.L + 2 * (size_t)p.L + 2 * (size_t)ntok * p.K) * sizeof(int32_t);
 }
 __host__ __device__ inline size_t stage_offset(const ScatterArgs& p, int64_t ntok) {
   return (layout_bytes(p, ntok) + 127) / 128 * 128;
@@ -101,6 +102,7 @@ __device__ inline int64_t ntok_smem(const ScatterArgs& p) {
 
 template <int GSZ, int FMT>
 __device__ __forceinline__ void store_scales(const ScatterArgs& p, int nslots, const int* rows,
+                                             const int* exps,
                                              int lane, bool active, int e, float sval,
                                              int group_base, int G, int G4) {
   constexpr int GL = GSZ / 16;  // lanes per group
@@ -121,8 +123,8 @@ __device__ __forceinline__ void store_scales(const ScatterArgs& p, int nslots, c
         const int row = rows[k];
         if (row < 0) continue;
         int64_t pk = row;  // compact / identity: one block
-        if (p.mode == kModeMasked) {
-          const int ex = row / p.cap;
+        if (p.mode == kModeMasked) {  // one block per expert (no division: the expert is kept)
+          const int ex = exps[k];
           pk = (int64_t)ex * G4 * p.ld_s + (row - ex * p.cap);
         }
         sc[pk + wofs] = word;
@@ -333,6 +335,7 @@ __global__ void __launch_bounds__(1024, MOEPERM_SCATTER_MIN_BLOCKS) quant_scatte
   uint8_t* stage = reinterpret_cast<uint8_t*>(sm) + stage_offset(p, ntok_smem(p));
   int32_t* pre_s = reinterpret_cast<int32_t*>(stage + (size_t)p.stages * H);  // [pre][kCPT][bd]
   int32_t* rows_s = sm;  // identity mode: unused
+  int32_t* exps_s = sm;  // expert of each slot (masked scale blocks)
   int32_t* st = sm;
   int32_t* ps = sm;
   int npre = 0;
@@ -369,6 +372,7 @@ __global__ void __launch_bounds__(1024, MOEPERM_SCATTER_MIN_BLOCKS) quant_scatte
     st = tbl + p.nchunks * L;
     ps = st + L;
     rows_s = ps + L;
+    exps_s = rows_s + (size_t)ntok_smem(p) * p.K;
     layout_prologue(p, tbl, st, ps, s_wsum);
 
     // rows of every slot this CTA will scatter
@@ -388,6 +392,7 @@ __global__ void __launch_bounds__(1024, MOEPERM_SCATTER_MIN_BLOCKS) quant_scatte
       p.src2dst[a] = row;
       if (row >= 0 && p.row_weights != nullptr) p.row_weights[row] = __ldg(p.w + a);
       rows_s[i] = row;
+      exps_s[i] = e;
     }
     __syncthreads();
   }
@@ -409,6 +414,7 @@ __global__ void __launch_bounds__(1024, MOEPERM_SCATTER_MIN_BLOCKS) quant_scatte
     const int tn = t + gridDim.x;
     if (!staged) load_row(vn, tn < n_live ? p.x + (int64_t)tn * p.ldx : nullptr, nch, bd, tid);
     const int* rows;
+    const int* exps = exps_s + it * p.K;
     if (identity) {
       ident_row[0] = t;
       rows = ident_row;
@@ -433,7 +439,7 @@ __global__ void __launch_bounds__(1024, MOEPERM_SCATTER_MIN_BLOCKS) quant_scatte
       }
       const int cw = i * bd + (tid & ~31);  // first chunk of this warp
       if (cw < nch)
-        store_scales<GSZ, FMT>(p, nslots, rows, lane, active, e, sval, cw * 16 / GSZ, G, G4);
+        store_scales<GSZ, FMT>(p, nslots, rows, exps, lane, active, e, sval, cw * 16 / GSZ, G, G4);
     }
     fence_proxy_async_smem();
     if (tid == 0) wait_ring(p.stages);
