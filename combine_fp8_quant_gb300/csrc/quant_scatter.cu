@@ -69,10 +69,9 @@ constexpr int kPre = MOEPERM_SCATTER_PRE < kStages ? MOEPERM_SCATTER_PRE : kStag
 static_assert(kStages >= 2 && kStages <= 6, "staging ring of 2 to 6 rows");
 
 // Dynamic shared memory: [table nchunks*L | starts L | psum L | rows ntok*K |
-// experts ntok*K]
-// (dispatch modes only), then, at a 128-byte boundary, p.stages staged rows of
-// H bytes and the scales of the tokens staged early (p.pre x kCPT x threads
-// words).
+// experts ntok*K] (dispatch modes only), then, at a 128-byte boundary,
+// p.stages staged rows of H bytes and the scales of the tokens staged early
+// (p.pre x kCPT x threads words).
 __host__ __device__ inline size_t layout_bytes(const ScatterArgs& p, int64_t ntok) {
   if (p.mode == kModeIdentity) return 0;
   return ((size_t)p.nchunks * p.L + 2 * (size_t)p.L + 2 * (size_t)ntok * p.K) * sizeof(int32_t);
@@ -102,9 +101,8 @@ __device__ inline int64_t ntok_smem(const ScatterArgs& p) {
 
 template <int GSZ, int FMT>
 __device__ __forceinline__ void store_scales(const ScatterArgs& p, int nslots, const int* rows,
-                                             const int* exps,
-                                             int lane, bool active, int e, float sval,
-                                             int group_base, int G, int G4) {
+                                             const int* exps, int lane, bool active, int e,
+                                             float sval, int group_base, int G, int G4) {
   constexpr int GL = GSZ / 16;  // lanes per group
   constexpr int GPW = 32 / GL;  // groups per warp
   const uint32_t byte = active ? (uint32_t)(e + 127) : 0u;
