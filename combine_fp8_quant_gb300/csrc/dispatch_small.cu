@@ -25,6 +25,7 @@
 //      converts) and store each 16-byte vector to every destination row.
 #include "common.cuh"
 #include "kernels.h"
+#include "scales.cuh"
 
 namespace moeperm {
 
@@ -34,62 +35,6 @@ constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kCPT = 2;
 
-template <int GSZ, int FMT>
-__device__ __forceinline__ void small_store_scales(const ScatterArgs& p, const int* rows,
-                                                   const int* exps, int nslots,
-                                                   int lane, bool active, int e, float sval,
-                                                   int group_base, int G, int G4) {
-  constexpr int GL = GSZ / 16;
-  constexpr int GPW = 32 / GL;
-  const uint32_t byte = active ? (uint32_t)(e + 127) : 0u;
-  const int gidx = group_base + lane / GL;
-  const bool leader = active && (lane % GL) == 0;
-  if constexpr (FMT == kFmtPacked) {
-    const uint32_t word = __shfl_sync(0xffffffffu, byte, 0) |
-                          (__shfl_sync(0xffffffffu, byte, 8) << 8) |
-                          (__shfl_sync(0xffffffffu, byte, 16) << 16) |
-                          (__shfl_sync(0xffffffffu, byte, 24) << 24);
-    if (lane == 0 && active) {
-      const int64_t wofs = (int64_t)(group_base / 4) * p.ld_s;
-      uint32_t* sc = reinterpret_cast<uint32_t*>(p.scales);
-      for (int k = 0; k < nslots; ++k) {
-        const int row = rows[k];
-        if (row < 0) continue;
-        int64_t pk = row;
-        if (p.mode == kModeMasked) {
-          const int ex = exps[k];  // masked: one scale block per expert
-          pk = (int64_t)ex * G4 * p.ld_s + (row - ex * p.cap);
-        }
-        sc[pk + wofs] = word;
-      }
-    }
-  } else if constexpr (FMT == kFmtU8 || FMT == kFmtMX) {
-    constexpr int WPW = GPW / 4;
-    const int q = lane % WPW;
-    uint32_t word = 0;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) word |= __shfl_sync(0xffffffffu, byte, (4 * q + j) * GL) << (8 * j);
-    const bool word_ok = (p.ld_s % 4) == 0;
-    uint8_t* sc = reinterpret_cast<uint8_t*>(p.scales);
-    if (word_ok && lane < WPW && group_base + 4 * q + 3 < G) {
-      for (int k = 0; k < nslots; ++k)
-        if (rows[k] >= 0)
-          *reinterpret_cast<uint32_t*>(sc + (int64_t)rows[k] * p.ld_s + group_base + 4 * q) = word;
-    }
-    const bool by_word = word_ok && ((gidx / 4) * 4 + 3 < G);
-    if (leader && !by_word) {
-      for (int k = 0; k < nslots; ++k)
-        if (rows[k] >= 0) sc[(int64_t)rows[k] * p.ld_s + gidx] = (uint8_t)byte;
-    }
-  } else {
-    if (leader) {
-      float* sc = reinterpret_cast<float*>(p.scales);
-      const float v = (FMT == kFmtF32) ? sval : __uint_as_float((uint32_t)(e + 127) << 23);
-      for (int k = 0; k < nslots; ++k)
-        if (rows[k] >= 0) sc[(int64_t)rows[k] * p.ld_s + gidx] = v;
-    }
-  }
-}
 
 template <int GSZ, int FMT, int S>
 __global__ void __launch_bounds__(kThreads) dispatch_small_kernel(ScatterArgs p) {
@@ -298,7 +243,7 @@ __global__ void __launch_bounds__(kThreads) dispatch_small_kernel(ScatterArgs p)
           }
         const int cw = c0 + i * kThreads + (tid & ~31);
         if (cw < nch)
-          small_store_scales<GSZ, FMT>(p, rows, exps, K, lane, active, e, sval, cw * 16 / GSZ, G, G4);
+          store_scales<GSZ, FMT>(p, K, rows, exps, lane, active, e, sval, cw * 16 / GSZ, G, G4);
       }
     }
   }

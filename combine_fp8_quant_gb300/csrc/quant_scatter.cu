@@ -43,6 +43,7 @@
 //   128) per destination.
 #include "common.cuh"
 #include "kernels.h"
+#include "scales.cuh"
 
 namespace moeperm {
 
@@ -99,62 +100,6 @@ __device__ inline int64_t ntok_smem(const ScatterArgs& p) {
   return ((int64_t)p.T + gridDim.x - 1) / gridDim.x;
 }
 
-template <int GSZ, int FMT>
-__device__ __forceinline__ void store_scales(const ScatterArgs& p, int nslots, const int* rows,
-                                             const int* exps, int lane, bool active, int e,
-                                             float sval, int group_base, int G, int G4) {
-  constexpr int GL = GSZ / 16;  // lanes per group
-  constexpr int GPW = 32 / GL;  // groups per warp
-  const uint32_t byte = active ? (uint32_t)(e + 127) : 0u;
-  const int gidx = group_base + lane / GL;
-  const bool leader = active && (lane % GL) == 0;
-  if constexpr (FMT == kFmtPacked) {
-    static_assert(GSZ == 128, "packed layout is defined for groups of 128");
-    const uint32_t word = __shfl_sync(0xffffffffu, byte, 0) |
-                          (__shfl_sync(0xffffffffu, byte, 8) << 8) |
-                          (__shfl_sync(0xffffffffu, byte, 16) << 16) |
-                          (__shfl_sync(0xffffffffu, byte, 24) << 24);
-    if (lane == 0 && active) {
-      const int64_t wofs = (int64_t)(group_base / 4) * p.ld_s;
-      uint32_t* sc = reinterpret_cast<uint32_t*>(p.scales);
-      for (int k = 0; k < nslots; ++k) {
-        const int row = rows[k];
-        if (row < 0) continue;
-        int64_t pk = row;  // compact / identity: one block
-        if (p.mode == kModeMasked) {  // one block per expert (no division: the expert is kept)
-          const int ex = exps[k];
-          pk = (int64_t)ex * G4 * p.ld_s + (row - ex * p.cap);
-        }
-        sc[pk + wofs] = word;
-      }
-    }
-  } else if constexpr (FMT == kFmtU8 || FMT == kFmtMX) {
-    constexpr int WPW = GPW / 4;  // whole 4-group words per warp
-    const int q = lane % WPW;
-    uint32_t word = 0;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) word |= __shfl_sync(0xffffffffu, byte, (4 * q + j) * GL) << (8 * j);
-    const bool word_ok = (p.ld_s % 4) == 0;
-    uint8_t* sc = reinterpret_cast<uint8_t*>(p.scales);
-    if (word_ok && lane < WPW && group_base + 4 * q + 3 < G) {
-      for (int k = 0; k < nslots; ++k)
-        if (rows[k] >= 0)
-          *reinterpret_cast<uint32_t*>(sc + (int64_t)rows[k] * p.ld_s + group_base + 4 * q) = word;
-    }
-    const bool by_word = word_ok && ((gidx / 4) * 4 + 3 < G);
-    if (leader && !by_word) {
-      for (int k = 0; k < nslots; ++k)
-        if (rows[k] >= 0) sc[(int64_t)rows[k] * p.ld_s + gidx] = (uint8_t)byte;
-    }
-  } else {  // fp32 scales: 2^e, or the plain amax / 448
-    if (leader) {
-      float* sc = reinterpret_cast<float*>(p.scales);
-      const float v = (FMT == kFmtF32) ? sval : __uint_as_float((uint32_t)(e + 127) << 23);
-      for (int k = 0; k < nslots; ++k)
-        if (rows[k] >= 0) sc[(int64_t)rows[k] * p.ld_s + gidx] = v;
-    }
-  }
-}
 
 __device__ __forceinline__ void load_row(uint4 (&v)[kCPT][2], const uint16_t* xrow, int nch,
                                          int bd, int tid) {
