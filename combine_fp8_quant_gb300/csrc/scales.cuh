@@ -19,8 +19,6 @@ __device__ __forceinline__ void store_scales(const ScatterArgs& p, int nslots, c
   constexpr int GL = GSZ / 16;  // lanes per group
   constexpr int GPW = 32 / GL;  // groups per warp
   const uint32_t byte = active ? (uint32_t)(e + 127) : 0u;
-  const int gidx = group_base + lane / GL;
-  const bool leader = active && (lane % GL) == 0;
   if constexpr (FMT == kFmtPacked) {
     static_assert(GSZ == 128, "packed layout is defined for groups of 128");
     const uint32_t word = __shfl_sync(0xffffffffu, byte, 0) |
@@ -56,17 +54,24 @@ __device__ __forceinline__ void store_scales(const ScatterArgs& p, int nslots, c
         if (rows[k] >= 0)
           *reinterpret_cast<uint32_t*>(sc + (int64_t)rows[k] * p.ld_s + group_base + 4 * q) = word;
     }
+    // otherwise byte by byte, from the first lane of each group
+    const int gidx = group_base + lane / GL;
     const bool by_word = word_ok && ((gidx / 4) * 4 + 3 < G);
-    if (leader && !by_word) {
+    if (active && (lane % GL) == 0 && !by_word) {
       for (int k = 0; k < nslots; ++k)
         if (rows[k] >= 0) sc[(int64_t)rows[k] * p.ld_s + gidx] = (uint8_t)byte;
     }
   } else {  // fp32 scales: 2^e, or the plain amax / 448
-    if (leader) {
+    // lane = (destination, group): group q of destination k on lane q + GPW * k,
+    // the value taken from the group's first lane
+    const float mine = (FMT == kFmtF32) ? sval : __uint_as_float((uint32_t)(e + 127) << 23);
+    const int q = lane % GPW;
+    const float v = __shfl_sync(0xffffffffu, mine, q * GL);
+    const bool q_active = __shfl_sync(0xffffffffu, (int)active, q * GL) != 0;
+    if (q_active) {
       float* sc = reinterpret_cast<float*>(p.scales);
-      const float v = (FMT == kFmtF32) ? sval : __uint_as_float((uint32_t)(e + 127) << 23);
-      for (int k = 0; k < nslots; ++k)
-        if (rows[k] >= 0) sc[(int64_t)rows[k] * p.ld_s + gidx] = v;
+      for (int k = lane / GPW; k < nslots; k += 32 / GPW)
+        if (rows[k] >= 0) sc[(int64_t)rows[k] * p.ld_s + group_base + q] = v;
     }
   }
 }
