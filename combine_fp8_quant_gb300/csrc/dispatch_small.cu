@@ -269,10 +269,12 @@ cudaError_t launch_s(const ScatterArgs& a, int num_sms, cudaStream_t s) {
 template <int GSZ, int FMT>
 cudaError_t launch_f(const ScatterArgs& a, int num_sms, cudaStream_t s) {
   const int64_t A = (int64_t)a.T * a.K;
+  static_assert(kWarps * 32 * 16 == kSmallSlotsMax, "ranking capacity of one CTA");
+  if (A > kSmallSlotsMax) return cudaErrorInvalidValue;  // slots past the capacity would stay unranked
   if (A <= 256) return launch_s<GSZ, FMT, 1>(a, num_sms, s);
   if (A <= 1024) return launch_s<GSZ, FMT, 4>(a, num_sms, s);
   if (A <= 2048) return launch_s<GSZ, FMT, 8>(a, num_sms, s);
-  return launch_s<GSZ, FMT, 16>(a, num_sms, s);  // only if the threshold is raised (<= 4096)
+  return launch_s<GSZ, FMT, 16>(a, num_sms, s);
 }
 
 }  // namespace

@@ -75,6 +75,9 @@ cudaError_t launch_quant_scatter(const ScatterArgs& a, int g, int fmt, int num_s
 #define MOEPERM_SMALL_SLOTS 2048
 #endif
 constexpr int64_t kSmallSlots = MOEPERM_SMALL_SLOTS;
+// The one-launch kernel ranks at most 8 warps x 32 lanes x 16 steps slots.
+constexpr int64_t kSmallSlotsMax = 4096;
+static_assert(kSmallSlots <= kSmallSlotsMax, "the one-launch dispatch ranks at most 4096 slots");
 cudaError_t launch_dispatch_small(const ScatterArgs& a, int g, int fmt, int num_sms,
                                   cudaStream_t s);
 
