@@ -336,10 +336,56 @@ def combine(y, src2dst, weights=None, num_tokens=None, status=None, out=None):
     return out
 
 
-def requant(q, s_tok):
-    """Per-token -> per-tensor e4m3 requant. Returns (q_out uint8 [T,H], S [1] f32)."""
+def expand_to_slab(exp, psum, num_local_experts, cap, align=128, exp_scales=None, ld_es=0,
+                   scale_fmt="packed", group_size=128, status=None):
+    """Expanded rows (e4m3 as uint8 / float8, or bfloat16 [R, H]) with segment
+    ends psum [L] -> per-expert slabs [L, cap, H]; the scales follow when
+    exp_scales is given. Returns a dict (slab, scales, ld_s, masked_m, status)."""
+    R, H = exp.shape
+    L = num_local_experts
+    dev = exp.device
+    slab = torch.empty((L, cap, H), dtype=exp.dtype, device=dev)
+    ssc, ld_ss = (scale_tensor(scale_fmt, L * cap, H, group_size, dev, blocks=L)
+                  if exp_scales is not None else (None, 0))
+    masked_m = torch.empty(L, dtype=torch.int32, device=dev)
+    st = status if status is not None else torch.zeros(1, dtype=torch.int32, device=dev)
+    _check(moe_expand_to_slab(exp, exp.element_size(), H, R, exp_scales, ld_es, psum, L, align,
+                              cap, scale_fmt, group_size, slab, ssc, ld_ss, masked_m, st),
+           "moe_expand_to_slab")
+    return dict(slab=slab, scales=ssc, ld_s=ld_ss, masked_m=masked_m, status=st)
+
+
+def expand_from_slab(slab, psum, num_rows, align=128, slab_scales=None, ld_ss=0,
+                     scale_fmt="packed", group_size=128, row_weights=None, status=None,
+                     m_indices=True):
+    """Per-expert slabs [L, cap, H] -> expanded rows [num_rows, H] at the
+    segment ends psum [L]; bfloat16 rows are scaled by row_weights when given.
+    Returns a dict (exp, scales, ld_s, m_indices, status)."""
+    L, cap, H = slab.shape
+    dev = slab.device
+    exp = torch.empty((num_rows, H), dtype=slab.dtype, device=dev)
+    esc, ld_es = (scale_tensor(scale_fmt, num_rows, H, group_size, dev)
+                  if slab_scales is not None else (None, 0))
+    mi = torch.empty(num_rows, dtype=torch.int32, device=dev) if m_indices else None
+    st = status if status is not None else torch.zeros(1, dtype=torch.int32, device=dev)
+    _check(moe_expand_from_slab(slab, slab.element_size(), H, slab_scales, ld_ss, psum, L, align,
+                                cap, scale_fmt, group_size, row_weights, exp, num_rows, esc,
+                                ld_es, mi, st), "moe_expand_from_slab")
+    return dict(exp=exp, scales=esc, ld_s=ld_es, m_indices=mi, status=st)
+
+
+def requant(q, s_tok, s_fmt="f32", mode="max_scale"):
+    """Per-token -> per-tensor e4m3 requant. s_tok: fp32 [T] ("f32") or e8m0
+    bytes [T] ("ue8m0"); mode "max_scale" (S = max s) or "amax" (S = max of
+    s * row amax / 448). Returns (q_out uint8 [T,H], S [1] f32)."""
     T, H = q.shape
     q_out = torch.empty((T, H), dtype=torch.uint8, device=q.device)
     S = torch.empty(1, dtype=torch.float32, device=q.device)
-    _check(fp8_requant_per_tensor(q, q.stride(0), s_tok, T, H, q_out, S), "fp8_requant_per_tensor")
+    if s_fmt == "f32" and mode == "max_scale":
+        _check(fp8_requant_per_tensor(q, q.stride(0), s_tok, T, H, q_out, S),
+               "fp8_requant_per_tensor")
+    else:
+        ws = torch.empty(max(T, 1), dtype=torch.float32, device=q.device)
+        _check(fp8_requant_per_tensor_ex(q, q.stride(0), s_tok, s_fmt, T, H, mode, q_out, S, ws,
+                                         ws.numel() * 4), "fp8_requant_per_tensor_ex")
     return q_out, S

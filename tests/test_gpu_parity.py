@@ -558,6 +558,61 @@ def test_repack_bad_layout_flagged(dev, ref):
         assert int(st.item()) & dev.STATUS_BAD_LAYOUT
 
 
+def test_binding_allocating_wrappers_repack_and_requant(dev, ref):
+    """The allocating wrappers of the binding: quant_group -> expand_to_slab ->
+    expand_from_slab round trip (e4m3 rows with packed scales, and weighted
+    bf16 rows) against the oracle, and requant in each scale format / mode."""
+    rng = np.random.default_rng(77)
+    counts = [3, 0, 140, 1, 30]
+    H, g, align, cap, L = 1024, 128, 128, 256, len(counts)
+    psum, starts, R = build_layout(counts, align)
+    x = synth.normal_bf16(rng, (R, H), outlier_frac=0.02)
+    q = dev.quant_group(bf16_dev(x), group_size=g, scale_fmt="packed")
+    fwd = dev.expand_to_slab(q["xq"], to_dev(psum), L, cap, align=align, exp_scales=q["scales"],
+                             ld_es=q["ld_s"], scale_fmt="packed", group_size=g)
+    back = dev.expand_from_slab(fwd["slab"], to_dev(psum), R, align=align,
+                                slab_scales=fwd["scales"], ld_ss=fwd["ld_s"], scale_fmt="packed",
+                                group_size=g)
+    torch.cuda.synchronize()
+    exp = np.zeros((R, H), np.uint8)
+    esc, ld_es = ref.scale_buffer("packed", R, H // g, fill=0)
+    ref.quant_group(x, R, R, H, g, "packed", exp, esc, ld_es)
+    real = np.concatenate([np.arange(s0, s0 + c) for s0, c in zip(starts, counts)])
+    assert np.array_equal(back["exp"].cpu().numpy()[real], exp[real])
+    assert np.array_equal(fwd["masked_m"].cpu().numpy(), np.minimum(counts, cap))
+    mi_want = np.full(R, -1, np.int32)
+    for e, (s0, c) in enumerate(zip(starts, counts)):
+        mi_want[s0:s0 + c] = e
+    assert np.array_equal(back["m_indices"].cpu().numpy(), mi_want)
+    got_sc = back["scales"].cpu().numpy().reshape(-1, back["ld_s"])[:, real]
+    assert np.array_equal(got_sc, esc.view(np.int32).reshape(-1, ld_es)[:, real])
+    # weighted bf16 rows
+    yb = synth.normal_bf16(rng, (R, H))
+    wts = rng.random(R).astype(np.float32)
+    fwd2 = dev.expand_to_slab(bf16_dev(yb), to_dev(psum), L, cap, align=align)
+    back2 = dev.expand_from_slab(fwd2["slab"], to_dev(psum), R, align=align, row_weights=to_dev(wts))
+    torch.cuda.synchronize()
+    want = np.full((R, 2 * H), 0, np.uint8)
+    slab = np.full((L * cap, 2 * H), 0, np.uint8)
+    mm = np.zeros(L, np.int32)
+    ref.expand_to_slab(yb.view(np.uint8).reshape(R, 2 * H), 2, H, R, None, 0, psum, L, align, cap,
+                       "u8", g, slab, None, 0, mm)
+    mi = np.zeros(R, np.int32)
+    ref.expand_from_slab(slab, 2, H, None, 0, psum, L, align, cap, "u8", g, wts, want, R, None, 0, mi)
+    got = back2["exp"].view(torch.int16).cpu().numpy().view(np.uint8).reshape(R, 2 * H)
+    assert np.array_equal(got[real], want[real])
+    # requant, every scale format and mode
+    dq = synth.requant(9, T=64, H=H)
+    s8 = np.random.default_rng(5).integers(100, 150, size=64).astype(np.uint8)
+    for s_fmt, s_tok in (("f32", dq["s_tok"]), ("ue8m0", s8)):
+        for mode in ("max_scale", "amax"):
+            qo, S = dev.requant(to_dev(dq["q"]), to_dev(s_tok), s_fmt=s_fmt, mode=mode)
+            torch.cuda.synchronize()
+            want_q, want_S = ref.requant_ex(dq["q"], s_tok, 64, H, s_fmt, mode)
+            assert np.array_equal(qo.cpu().numpy(), want_q), (s_fmt, mode)
+            assert float(S.item()) == want_S
+
+
 # ---------------------------------------------------------------------------
 # requant
 # ---------------------------------------------------------------------------
