@@ -53,6 +53,21 @@ MUTANTS = [
      "int64_t src = start[e] + j, dst = (int64_t)e * cap + (cap - 1 - j);", ["test_repack_roundtrip"]),
     ("masked_m_unclamped", "masked_m[e] = counts[e] < cap ? counts[e] : cap;", "masked_m[e] = counts[e];",
      ["test_dispatch_masked_overflow"]),
+    # widened rows: OCP-MX exponent, plain fp32 scales, e8m0 / amax requant, weighted repack
+    ("mx_emax_off_by_one", "  int X = k - 8;", "  int X = k - 7;",
+     ["test_mx_exponent_closed_forms_and_interval", "test_quant_row_mx_against_library"]),
+    ("f32_scale_divisor", "      float sc = a / 448.0f;", "      float sc = a / 240.0f;",
+     ["test_quant_row_f32_against_library"]),
+    ("f32_quotient_inverted", "        float v = (float)bf16_value(x[h]) / sc;",
+     "        float v = (float)bf16_value(x[h]) * sc;", ["test_quant_row_f32_against_library"]),
+    ("requant_amax_drops_token_scale", "      v = s[t] * (float)amax;", "      v = (float)amax;",
+     ["test_requant_ex_amax_mode_against_library"]),
+    ("requant_amax_divisor", "  if (mode == 1) S = S / 448.0f;", "  if (mode == 1) S = S / 240.0f;",
+     ["test_requant_ex_amax_mode_against_library"]),
+    ("e8m0_decode_bias", "(int)((const uint8_t*)s_tok)[t] - 127);", "(int)((const uint8_t*)s_tok)[t] - 128);",
+     ["test_requant_ex_ue8m0_scales_are_exact_powers"]),
+    ("repack_weight_ignored", "d16[h] = ref_bf16_rne(wr * (float)bf16_value(s16[h]));",
+     "d16[h] = ref_bf16_rne((float)bf16_value(s16[h]));", ["test_repack_weighted_rows"]),
 ]
 
 
@@ -81,6 +96,8 @@ def run_pin(name):
         fn(oracle, "packed")
     elif "g" in params:
         fn(oracle, 128, 640)
+    elif "H" in params:
+        fn(oracle, 224)
     else:
         fn(oracle)
 
