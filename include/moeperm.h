@@ -176,10 +176,12 @@ size_t moe_workspace_bytes(int32_t T, int32_t K, int32_t L);
  * are the exclusive prefix sums of the aligned counts.
  * Limits: T*K <= 2^20, H <= 32768, and the chunk table within 64 KiB.
  * Workspace: moe_workspace_bytes(T, K, L) bytes (no initialisation needed).
- * Launches: 2, fixed grids -- the route plan (chunk histograms and stable
- * ranks), then the layout + quantise + scatter + m_indices launch, which is
- * started early with programmatic dependent launch and waits for the route
- * plan's results on the device.
+ * Launches (fixed grids, the same results either way): for T*K <= 2048
+ * slots, one launch in which every CTA ranks all slots in shared memory;
+ * otherwise two -- the route plan (chunk histograms and stable ranks), then
+ * the layout + quantise + scatter + m_indices launch. The second is started
+ * early with programmatic dependent launch: its CTAs quantise their first
+ * tokens while the route plan runs and wait for its results on the device.
  */
 moe_status_t moe_dispatch_compact(
     const void* x, int64_t ldx, int32_t T, const int32_t* d_num_tokens, int32_t H,
