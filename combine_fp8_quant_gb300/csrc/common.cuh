@@ -174,6 +174,33 @@ __device__ __forceinline__ void bulk_store_s2g(void* gdst, uint32_t ssrc, uint32
                ::"l"(gdst), "r"(ssrc), "r"(bytes)
                : "memory");
 }
+// Same, with an L2 cache policy (from createpolicy) on the written lines.
+__device__ __forceinline__ void bulk_store_s2g_hint(void* gdst, uint32_t ssrc, uint32_t bytes,
+                                                    uint64_t policy) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;"
+               ::"l"(gdst), "r"(ssrc), "r"(bytes), "l"(policy)
+               : "memory");
+}
+// Bulk (TMA) prefetch of `bytes` of global memory into L2 (16-byte aligned
+// address, bytes a multiple of 16); nothing waits for it.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* g, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(g), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void bulk_prefetch_l2_hint(const void* g, uint32_t bytes, uint64_t policy) {
+  asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;"
+               ::"l"(g), "r"(bytes), "l"(policy)
+               : "memory");
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }

@@ -61,6 +61,18 @@ namespace {
 #ifndef MOEPERM_SCATTER_MIN_BLOCKS
 #define MOEPERM_SCATTER_MIN_BLOCKS 1
 #endif
+// Tokens ahead of the register prefetch whose x rows thread 0 prefetches
+// into L2 with a bulk prefetch (0: none), and L2 policies for those lines
+// (evict_last) and for the payload rows written (evict_first).
+#ifndef MOEPERM_SCATTER_L2PF
+#define MOEPERM_SCATTER_L2PF 0
+#endif
+#ifndef MOEPERM_SCATTER_PF_HINT
+#define MOEPERM_SCATTER_PF_HINT 0
+#endif
+#ifndef MOEPERM_SCATTER_ST_HINT
+#define MOEPERM_SCATTER_ST_HINT 1
+#endif
 constexpr int kCPT = MOEPERM_SCATTER_CPT;          // 16-element chunks per thread
 // Largest staging ring (rows in flight to the bulk-copy engine) and number of
 // tokens quantised before the wait on the route plan; the launch lowers both
@@ -70,12 +82,13 @@ constexpr int kPre = MOEPERM_SCATTER_PRE < kStages ? MOEPERM_SCATTER_PRE : kStag
 static_assert(kStages >= 2 && kStages <= 6, "staging ring of 2 to 6 rows");
 
 // Dynamic shared memory: [table nchunks*L | starts L | psum L | rows ntok*K |
-// experts ntok*K] (dispatch modes only), then, at a 128-byte boundary,
+// experts ntok*K | token list ntok] (dispatch modes only), then, at a 128-byte boundary,
 // p.stages staged rows of H bytes and the scales of the tokens staged early
 // (p.pre x kCPT x threads words).
 __host__ __device__ inline size_t layout_bytes(const ScatterArgs& p, int64_t ntok) {
   if (p.mode == kModeIdentity) return 0;
-  return ((size_t)p.nchunks * p.L + 2 * (size_t)p.L + 2 * (size_t)ntok * p.K) * sizeof(int32_t);
+  return ((size_t)p.nchunks * p.L + 2 * (size_t)p.L + 2 * (size_t)ntok * p.K + (size_t)ntok) *
+         sizeof(int32_t);
 }
 __host__ __device__ inline size_t stage_offset(const ScatterArgs& p, int64_t ntok) {
   return (layout_bytes(p, ntok) + 127) / 128 * 128;
@@ -252,6 +265,7 @@ template <int GSZ, int FMT>
 __global__ void __launch_bounds__(1024, MOEPERM_SCATTER_MIN_BLOCKS) quant_scatter_kernel(ScatterArgs p) {
   extern __shared__ int32_t sm[];
   __shared__ int32_t s_wsum[32];
+  __shared__ int32_t s_nlist;
   const int tid = threadIdx.x, lane = tid & 31, bd = blockDim.x;
   const int H = p.H;
   const int nch = H / 16;
@@ -279,6 +293,8 @@ __global__ void __launch_bounds__(1024, MOEPERM_SCATTER_MIN_BLOCKS) quant_scatte
   int32_t* pre_s = reinterpret_cast<int32_t*>(stage + (size_t)p.stages * H);  // [pre][kCPT][bd]
   int32_t* rows_s = sm;  // identity mode: unused
   int32_t* exps_s = sm;  // expert of each slot (masked scale blocks)
+  int32_t* list_s = sm;  // iteration -> token index of this CTA (dispatch modes)
+  int nlist = ntok;
   int32_t* st = sm;
   int32_t* ps = sm;
   int npre = 0;
@@ -289,7 +305,7 @@ __global__ void __launch_bounds__(1024, MOEPERM_SCATTER_MIN_BLOCKS) quant_scatte
     npre = ntok < p.pre ? ntok : p.pre;
     for (int j = 0; j < npre; ++j) {
       uint4 vn[kCPT][2];
-      load_row(vn, j + 1 < ntok ? p.x + (int64_t)(blockIdx.x + (j + 1) * gridDim.x) * p.ldx : nullptr,
+      load_row(vn, j + 1 < npre ? p.x + (int64_t)(blockIdx.x + (j + 1) * gridDim.x) * p.ldx : nullptr,
                nch, bd, tid);
       uint8_t* sb = stage + (size_t)j * H;
 #pragma unroll
@@ -316,6 +332,7 @@ __global__ void __launch_bounds__(1024, MOEPERM_SCATTER_MIN_BLOCKS) quant_scatte
     ps = st + L;
     rows_s = ps + L;
     exps_s = rows_s + (size_t)ntok_smem(p) * p.K;
+    list_s = exps_s + (size_t)ntok_smem(p) * p.K;
     layout_prologue(p, tbl, st, ps, s_wsum);
 
     // rows of every slot this CTA will scatter
@@ -338,6 +355,28 @@ __global__ void __launch_bounds__(1024, MOEPERM_SCATTER_MIN_BLOCKS) quant_scatte
       exps_s[i] = e;
     }
     __syncthreads();
+
+    // The tokens to walk: the staged ones, then, in order, every later token
+    // with at least one kept slot. A token whose experts are all remote is
+    // neither read nor quantised.
+    if (tid < 32) {
+      int base = npre;
+      for (int t0 = npre; t0 < ntok; t0 += 32) {
+        const int it = t0 + lane;
+        bool kept = false;
+        if (it < ntok)
+          for (int k = 0; k < p.K; ++k) kept |= rows_s[it * p.K + k] >= 0;
+        const unsigned m = __ballot_sync(0xffffffffu, kept);
+        if (kept) list_s[base + __popc(m & ((1u << lane) - 1u))] = it;
+        base += __popc(m);
+      }
+      if (lane == 0) s_nlist = base;
+    }
+    for (int j = tid; j < npre; j += bd) list_s[j] = j;
+    __syncthreads();
+    nlist = s_nlist;
+    if (npre == 0 && nlist > 0)  // no early tokens (shared memory was short): load the first one
+      load_row(v, p.x + (int64_t)(blockIdx.x + list_s[0] * gridDim.x) * p.ldx, nch, bd, tid);
   }
 
   // ---- token loop ---------------------------------------------------------
@@ -350,12 +389,30 @@ __global__ void __launch_bounds__(1024, MOEPERM_SCATTER_MIN_BLOCKS) quant_scatte
   // scales stored here.
   const uint32_t stage_s = (uint32_t)__cvta_generic_to_shared(stage);
   int ident_row[1];
-  for (int it = 0; it < ntok; ++it) {
+  uint64_t pf_policy = 0, st_policy = 0;
+  if (MOEPERM_SCATTER_PF_HINT) pf_policy = l2_policy_evict_last();
+  if (MOEPERM_SCATTER_ST_HINT) st_policy = l2_policy_evict_first();
+  auto prefetch_x = [&](int m) {  // list entry m, if it is one the loop will load
+    if (MOEPERM_SCATTER_L2PF > 0 && tid == 0 && m >= npre && m < nlist) {
+      const int itp = identity ? m : list_s[m];
+      const uint16_t* src = p.x + (int64_t)(blockIdx.x + itp * gridDim.x) * p.ldx;
+      if (MOEPERM_SCATTER_PF_HINT) bulk_prefetch_l2_hint(src, (uint32_t)(2 * H), pf_policy);
+      else bulk_prefetch_l2(src, (uint32_t)(2 * H));
+    }
+  };
+  for (int m = npre; m <= MOEPERM_SCATTER_L2PF; ++m) prefetch_x(m);
+  for (int n = 0; n < nlist; ++n) {
+    const int it = identity ? n : list_s[n];
     const int t = blockIdx.x + it * gridDim.x;
-    const bool staged = it < npre;
+    const bool staged = n < npre;  // the staged tokens are list entries 0 .. npre-1
+    const bool fetch = n + 1 >= npre;
+    prefetch_x(n + 1 + MOEPERM_SCATTER_L2PF);
     uint4 vn[kCPT][2];
-    const int tn = t + gridDim.x;
-    if (!staged) load_row(vn, tn < n_live ? p.x + (int64_t)tn * p.ldx : nullptr, nch, bd, tid);
+    if (fetch) {
+      const int itn = n + 1 < nlist ? (identity ? n + 1 : list_s[n + 1]) : -1;
+      load_row(vn, itn >= 0 ? p.x + (int64_t)(blockIdx.x + itn * gridDim.x) * p.ldx : nullptr,
+               nch, bd, tid);
+    }
     const int* rows;
     const int* exps = exps_s + it * p.K;
     if (identity) {
@@ -364,7 +421,7 @@ __global__ void __launch_bounds__(1024, MOEPERM_SCATTER_MIN_BLOCKS) quant_scatte
     } else {
       rows = rows_s + it * p.K;
     }
-    const int buf = it % p.stages;
+    const int buf = n % p.stages;
     uint8_t* sb = stage + (size_t)buf * H;
 #pragma unroll
     for (int i = 0; i < kCPT; ++i) {
@@ -390,11 +447,15 @@ __global__ void __launch_bounds__(1024, MOEPERM_SCATTER_MIN_BLOCKS) quant_scatte
     if (tid == 0) {
       for (int k = 0; k < nslots; ++k) {
         const int row = rows[k];
-        if (row >= 0) bulk_store_s2g(p.xq + (int64_t)row * H, stage_s + (uint32_t)(buf * H), (uint32_t)H);
+        if (row < 0) continue;
+        if (MOEPERM_SCATTER_ST_HINT)
+          bulk_store_s2g_hint(p.xq + (int64_t)row * H, stage_s + (uint32_t)(buf * H), (uint32_t)H, st_policy);
+        else
+          bulk_store_s2g(p.xq + (int64_t)row * H, stage_s + (uint32_t)(buf * H), (uint32_t)H);
       }
       bulk_commit();
     }
-    if (!staged) {
+    if (fetch) {
 #pragma unroll
       for (int i = 0; i < kCPT; ++i) {
         v[i][0] = vn[i][0];
