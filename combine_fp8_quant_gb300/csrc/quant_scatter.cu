@@ -29,8 +29,9 @@
 //   (one per thread). After the wait it loads the chunk table (<= 64 KiB)
 //   into shared memory, scans it, and resolves the rows of all of its own
 //   slots at once. The route plan therefore needs no serial "last block" and
-//   no fence. The m_indices fill runs after the token loop, while the last
-//   bulk copies drain.
+//   no fence. Tokens with no kept slot (all their experts remote) are dropped
+//   from the walk. The m_indices fill runs after the token loop, while the
+//   last bulk copies drain.
 //   Token loop: the next token's loads are issued before the current token is
 //   processed; the g/16 lanes of a group reduce the group max with xor
 //   shuffles on sign-cleared bf16 bit patterns; the exponent comes from the
@@ -38,9 +39,11 @@
 //   row is staged in shared memory and thread 0 writes it to each of the
 //   token's destination rows with one bulk (TMA) copy per row, so the payload
 //   -- 80% of the kernel's traffic -- leaves the SM as large asynchronous
-//   transfers instead of per-thread stores. Scales are small direct stores:
+//   transfers (with an evict_first L2 policy: nothing reads them back here)
+//   instead of per-thread stores. Scales are small direct stores:
 //   for the packed UE8M0 layout exactly one 32-bit word per warp (4 groups of
-//   128) per destination.
+//   128) per destination, the K destinations written from K lanes at once
+//   (scales.cuh).
 #include "common.cuh"
 #include "kernels.h"
 #include "scales.cuh"
