@@ -237,6 +237,21 @@ def test_dispatch_compact_nondividing_groups_and_dropped(dev, ref):
         compact_both(dev, ref, x, ids, w, H, K, 40, 20, 16, 128, fmt)
 
 
+@pytest.mark.parametrize("L", [32, 2])
+def test_dispatch_compact_sparse_two_launch(dev, ref, L):
+    """Two-launch compact dispatch where many tokens have no local expert
+    (top-8 over 256 experts with L local: ~34% of tokens for L = 32, ~94% for
+    L = 2). Such tokens are dropped from the scatter's walk; a CTA may be left
+    with only its early-staged tokens, or none with a kept slot."""
+    rng = np.random.default_rng(100 + L)
+    T, K, H = 700, 8, 1024
+    x = synth.normal_bf16(rng, (T, H))
+    ids = synth.uniform_topk(rng, T, 256, K)
+    w = synth.softmax_weights(rng, T, K)
+    for fmt in ("packed", "u8"):
+        compact_both(dev, ref, x, ids, w, H, K, 256, L, 128, 128, fmt)
+
+
 def test_dispatch_compact_live_tokens_and_stride(dev, ref):
     rng = np.random.default_rng(4)
     T, K, H, ldx = 200, 8, 1024, 1088
