@@ -389,6 +389,12 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     ms_disp_direct, ms_comb_direct = timed_steps(lambda: dispatch(x, ids), lambda: combine(y, w, out))
     ms_disp_direct, ms_comb_direct = max_over_ranks([ms_disp_direct, ms_comb_direct], world, dev)
+    # Each call alone after an L2 flush. Inside the step the combine starts
+    # while the dispatch's last payload writes (tens of MB) still drain from
+    # L2, so the step's split charges that write-back to the combine.
+    us_disp_alone = time_call(lambda: dispatch(x, ids), flush)
+    us_comb_alone = time_call(lambda: combine(y, w, out), flush)
+    us_disp_alone, us_comb_alone = max_over_ranks([us_disp_alone, us_comb_alone], world, dev)
     assert mp.moe_status_sync(st) == 0
 
     if args.only_step:
@@ -508,6 +514,12 @@ def run_ours(args, rank, world, local_rank):
                 "note": "the same steps through direct C-ABI calls instead of graph replays",
                 "dispatch_us": ms_disp_direct * 1e3, "combine_us": ms_comb_direct * 1e3,
                 "step_gbs": (db + cb) / ((ms_disp_direct + ms_comb_direct) * 1e-3) / 1e9},
+            "each_call_alone": {
+                "note": "each call timed on its own after an L2 flush (trimmed mean of 40); inside the "
+                        "step the combine also absorbs the write-back of the dispatch's last payload "
+                        "rows still dirty in L2",
+                "dispatch_us": us_disp_alone, "dispatch_gbs": db / (us_disp_alone * 1e-6) / 1e9,
+                "combine_us": us_comb_alone, "combine_gbs": cb / (us_comb_alone * 1e-6) / 1e9},
         },
         "roofline": {"bound": "hbm", "kernel": "combine_kernel", "achieved": comb_gbs, "peak": hbm,
                      "unit": "GB/s", "frac": comb_gbs / hbm, "traffic": traffic,
