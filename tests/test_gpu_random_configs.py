@@ -1,0 +1,85 @@
+"""GPU parity over seeded random configurations: dispatch (compact and
+masked), combine and repack against the CPU oracle over whole buffers, across
+token counts on both launch plans, top-k, local/total experts (ids outside the
+local range and dropped slots), hidden sizes, group sizes and scale layouts,
+block_e, device live counts, row strides and slab capacities (with and
+without overflow)."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from gpu_util import DEV, to_dev
+from test_gpu_parity import build_layout, check_combine, compact_both, masked_both, repack_both
+
+pytestmark = pytest.mark.gpu
+
+FMTS = {128: ["packed", "u8", "f32pow2", "f32"], 32: ["u8", "mx"]}
+
+
+def random_routing(rng, T, E, K):
+    ids = synth.uniform_topk(rng, T, E, K) if K <= E else rng.integers(0, E, size=(T, K)).astype(np.int32)
+    drop = rng.random((T, K)) < 0.05
+    ids[drop] = -1                                   # dropped slots
+    return ids
+
+
+def draw(rng):
+    g = int(rng.choice([128, 32]))
+    H = g * int(rng.integers(1, 9)) if g == 128 else 32 * int(rng.integers(1, 33))
+    T = int(rng.choice([int(rng.integers(1, 64)), int(rng.integers(300, 1500))]))   # one- and two-launch plans
+    K = int(rng.integers(1, 10))
+    L = int(rng.integers(1, 80))
+    E = L + int(rng.integers(0, 40))
+    fmt = str(rng.choice(FMTS[g]))
+    return g, H, T, K, L, E, fmt
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_compact_dispatch_and_combine(dev, ref, seed):
+    rng = np.random.default_rng(9000 + seed)
+    g, H, T, K, L, E, fmt = draw(rng)
+    b = int(rng.choice([1, 4, 16, 128]))
+    ldx = H + 16 * int(rng.integers(0, 3))
+    n_live = None if rng.random() < 0.5 else int(rng.integers(0, T + 1))
+    x = synth.normal_bf16(rng, (T, ldx), outlier_frac=0.01)
+    ids = random_routing(rng, T, E, K)
+    w = synth.softmax_weights(rng, T, K)
+    r, d, _ = compact_both(dev, ref, x, ids, w, H, K, E, L, b, g, fmt, n_live=n_live, ldx=ldx)
+    bound = ref.compact_bound(T * K, L, b)
+    y = synth.normal_bf16(rng, (max(bound, 1), H))
+    check_combine(dev, ref, y, r["s2d"], w, H, n_live=n_live)
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_random_masked_dispatch(dev, ref, seed):
+    rng = np.random.default_rng(9500 + seed)
+    g, H, T, K, L, E, fmt = draw(rng)
+    ids = random_routing(rng, T, E, K)
+    kept = ids[(ids >= 0) & (ids < L)]
+    top = int(np.bincount(kept, minlength=L).max()) if kept.size else 0
+    cap = max(1, top + int(rng.integers(-3, 4)))      # sometimes below the largest count: overflow
+    n_live = None if rng.random() < 0.5 else int(rng.integers(0, T + 1))
+    x = synth.normal_bf16(rng, (T, H), outlier_frac=0.01)
+    w = synth.softmax_weights(rng, T, K)
+    masked_both(dev, ref, x, ids, w, H, K, E, L, cap, g, fmt, n_live=n_live)
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_random_repack(dev, ref, seed):
+    rng = np.random.default_rng(9900 + seed)
+    L = int(rng.integers(1, 40))
+    align = int(rng.choice([1, 8, 128]))
+    counts = [int(c) if rng.random() < 0.8 else 0 for c in rng.integers(0, 300, size=L)]
+    psum, starts, R = build_layout(counts, align)
+    cap = max(1, max(counts) + int(rng.integers(-2, 3)))
+    eb = int(rng.choice([1, 2]))
+    H = 16 * int(rng.integers(1, 100))
+    if eb == 2:
+        exp = synth.normal_bf16(rng, (R, H)).view(np.uint8).reshape(R, 2 * H)
+        wts = rng.random(R).astype(np.float32) if rng.random() < 0.5 else None
+        repack_both(dev, ref, exp, 2, H, psum, L, align, cap, weights=wts)
+    else:
+        exp = rng.integers(0, 256, size=(R, H), dtype=np.uint8)
+        exp[(exp & 0x7F) == 0x7F] = 0x22
+        repack_both(dev, ref, exp, 1, H, psum, L, align, cap)
