@@ -692,6 +692,17 @@ def other_rows(mp, dev, flush):
     us = time_call(mx, flush)
     res["mxfp8_live_quant"] = entry(us, cm["n_live"] * cm["H"] * 3 + cm["n_live"] * 224)
     res["mxfp8_live_quant"]["capacity_rows"] = cm["T_cap"]
+    # the same quantiser on a full prefill batch (8192 rows, group 128, packed)
+    xf = torch.from_numpy(prefill_inputs(0)["x"].view(np.int16)).to(dev).view(torch.bfloat16)
+    Tq, Hq = xf.shape
+    xqf = torch.empty((Tq, Hq), dtype=torch.uint8, device=dev)
+    scf, ldf = mp.scale_tensor("packed", Tq, Hq, 128, dev)
+
+    def qf():
+        assert mp.moe_quant_group(xf, Hq, Tq, None, Hq, 128, "packed", xqf, scf, ldf, st) == 0
+    res["quant_group_prefill"] = entry(time_call(qf, flush), Tq * Hq * 3 + Tq * (Hq // 128))
+    res["quant_group_prefill"]["rows"] = Tq
+    del xf, xqf, scf
 
     # requant and expand <-> slab on the 4096-row workload, and on the same
     # rows tiled 4x (16384 rows, 4x the expert blocks): the small workload is

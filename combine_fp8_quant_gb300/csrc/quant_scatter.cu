@@ -16,7 +16,8 @@
 //   * compact only: m_indices over the whole static bound -- expert id on valid
 //     rows, -1 on padding rows and on the tail [PR #33128 _fwd_kernel_ep_scatter_1].
 //   The identity mode (row t -> row t, one slot) is the live-row quantiser of
-//   PR #36119: rows >= the device live count are never touched.
+//   PR #36119: rows >= the device live count are never touched. With a single
+//   destination per row it runs barrier-free with direct 16-byte stores.
 //
 // Design: a persistent grid (SMs x resident CTAs, independent of the routing)
 // walks the live tokens, t = blockIdx.x + i * gridDim.x. One thread owns two
@@ -97,6 +98,7 @@ __host__ __device__ inline size_t stage_offset(const ScatterArgs& p, int64_t nto
   return (layout_bytes(p, ntok) + 127) / 128 * 128;
 }
 __host__ __device__ inline size_t smem_bytes(const ScatterArgs& p, int64_t ntok, int bd) {
+  if (p.mode == kModeIdentity) return 0;  // direct stores, nothing staged
   return stage_offset(p, ntok) + (size_t)p.stages * p.H + (size_t)p.pre * kCPT * bd * sizeof(int32_t);
 }
 
@@ -380,6 +382,37 @@ __global__ void __launch_bounds__(1024, MOEPERM_SCATTER_MIN_BLOCKS) quant_scatte
     nlist = s_nlist;
     if (npre == 0 && nlist > 0)  // no early tokens (shared memory was short): load the first one
       load_row(v, p.x + (int64_t)(blockIdx.x + list_s[0] * gridDim.x) * p.ldx, nch, bd, tid);
+  }
+
+  // ---- identity mode (live-row quantiser): one destination per row, so no
+  // staging and no barrier. Every warp runs on its own: the next row's loads
+  // go out first, then the warp quantises its chunks and stores each 16-byte
+  // vector straight to the row (a warp writes 512 contiguous bytes).
+  if (identity) {
+    for (int it = 0; it < ntok; ++it) {
+      const int t = blockIdx.x + it * gridDim.x;
+      const int tn = t + gridDim.x;
+      uint4 vn[kCPT][2];
+      load_row(vn, tn < n_live ? p.x + (int64_t)tn * p.ldx : nullptr, nch, bd, tid);
+      const int rows[1] = {t};
+#pragma unroll
+      for (int i = 0; i < kCPT; ++i) {
+        const int c = i * bd + tid;
+        const bool active = c < nch;
+        int e;
+        float sval;
+        const uint4 qv = quant_chunk<GSZ, FMT>(v[i][0], v[i][1], e, sval);
+        if (active) st_v4(p.xq + (int64_t)t * H + c * 16, qv);
+        const int cw = i * bd + (tid & ~31);  // first chunk of this warp
+        if (cw < nch) store_scales<GSZ, FMT>(p, 1, rows, rows, lane, active, e, sval, cw * 16 / GSZ, G, G4);
+      }
+#pragma unroll
+      for (int i = 0; i < kCPT; ++i) {
+        v[i][0] = vn[i][0];
+        v[i][1] = vn[i][1];
+      }
+    }
+    return;
   }
 
   // ---- token loop ---------------------------------------------------------
