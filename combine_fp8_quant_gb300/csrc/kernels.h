@@ -45,6 +45,7 @@ struct ScatterArgs {
   const int32_t* ids;
   const float* w;
   int32_t K, L;
+  int32_t E;                   // all experts (the ids range over [0, E); local ones are [0, L))
   int32_t mode;
   int32_t block_e, cap;
   int32_t chunk, nchunks;
@@ -63,6 +64,7 @@ struct ScatterArgs {
   int32_t* masked_m;           // masked output [L]
   int32_t* status;
   int32_t stages, pre;         // scatter: staging ring size, tokens staged before the wait
+  int32_t direct;              // scatter: 1 = direct stores, no staging (few kept slots per token)
 };
 cudaError_t launch_quant_scatter(const ScatterArgs& a, int g, int fmt, int num_sms,
                                  bool after_route_plan, cudaStream_t s);

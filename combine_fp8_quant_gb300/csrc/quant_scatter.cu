@@ -17,7 +17,10 @@
 //     rows, -1 on padding rows and on the tail [PR #33128 _fwd_kernel_ep_scatter_1].
 //   The identity mode (row t -> row t, one slot) is the live-row quantiser of
 //   PR #36119: rows >= the device live count are never touched. With a single
-//   destination per row it runs barrier-free with direct 16-byte stores.
+//   destination per row it runs barrier-free with direct 16-byte stores, and
+//   so does a dispatch whose tokens keep few slots (K * L / E <= 3, decided on
+//   the host from scalars alone): there the per-token barrier of the staged
+//   path costs more than the bulk copies save.
 //
 // Design: a persistent grid (SMs x resident CTAs, independent of the routing)
 // walks the live tokens, t = blockIdx.x + i * gridDim.x. One thread owns two
@@ -77,6 +80,15 @@ namespace {
 #ifndef MOEPERM_SCATTER_ST_HINT
 #define MOEPERM_SCATTER_ST_HINT 1
 #endif
+// Direct stores instead of staging when few slots per token are kept: 1 =
+// always, 0 = never, -1 = when the expected kept slots per token, K * L / E
+// (uniform routing), are at most MOEPERM_SCATTER_DIRECT_FANOUT.
+#ifndef MOEPERM_SCATTER_DIRECT
+#define MOEPERM_SCATTER_DIRECT -1
+#endif
+#ifndef MOEPERM_SCATTER_DIRECT_FANOUT
+#define MOEPERM_SCATTER_DIRECT_FANOUT 3
+#endif
 constexpr int kCPT = MOEPERM_SCATTER_CPT;          // 16-element chunks per thread
 // Largest staging ring (rows in flight to the bulk-copy engine) and number of
 // tokens quantised before the wait on the route plan; the launch lowers both
@@ -99,6 +111,7 @@ __host__ __device__ inline size_t stage_offset(const ScatterArgs& p, int64_t nto
 }
 __host__ __device__ inline size_t smem_bytes(const ScatterArgs& p, int64_t ntok, int bd) {
   if (p.mode == kModeIdentity) return 0;  // direct stores, nothing staged
+  if (p.direct) return stage_offset(p, ntok);
   return stage_offset(p, ntok) + (size_t)p.stages * p.H + (size_t)p.pre * kCPT * bd * sizeof(int32_t);
 }
 
@@ -307,7 +320,7 @@ __global__ void __launch_bounds__(1024, MOEPERM_SCATTER_MIN_BLOCKS) quant_scatte
     // The first p.pre tokens are quantised into their staging buffers while the
     // route plan still runs (their rows are not known yet); their scales wait
     // in shared memory.
-    npre = ntok < p.pre ? ntok : p.pre;
+    npre = p.direct ? 0 : (ntok < p.pre ? ntok : p.pre);
     for (int j = 0; j < npre; ++j) {
       uint4 vn[kCPT][2];
       load_row(vn, j + 1 < npre ? p.x + (int64_t)(blockIdx.x + (j + 1) * gridDim.x) * p.ldx : nullptr,
@@ -380,7 +393,7 @@ __global__ void __launch_bounds__(1024, MOEPERM_SCATTER_MIN_BLOCKS) quant_scatte
     for (int j = tid; j < npre; j += bd) list_s[j] = j;
     __syncthreads();
     nlist = s_nlist;
-    if (npre == 0 && nlist > 0)  // no early tokens (shared memory was short): load the first one
+    if (npre == 0 && nlist > 0 && list_s[0] != 0)  // no early tokens: v holds token 0 already
       load_row(v, p.x + (int64_t)(blockIdx.x + list_s[0] * gridDim.x) * p.ldx, nch, bd, tid);
   }
 
@@ -413,6 +426,40 @@ __global__ void __launch_bounds__(1024, MOEPERM_SCATTER_MIN_BLOCKS) quant_scatte
       }
     }
     return;
+  }
+
+  // ---- direct mode: few kept slots per token, so no staging and no barrier;
+  // each warp stores its 16-byte vectors straight to every destination row.
+  if (p.direct) {
+    for (int n = 0; n < nlist; ++n) {
+      const int it = list_s[n];
+      const int itn = n + 1 < nlist ? list_s[n + 1] : -1;
+      uint4 vn[kCPT][2];
+      load_row(vn, itn >= 0 ? p.x + (int64_t)(blockIdx.x + itn * gridDim.x) * p.ldx : nullptr,
+               nch, bd, tid);
+      const int* rows = rows_s + it * p.K;
+      const int* exps = exps_s + it * p.K;
+#pragma unroll
+      for (int i = 0; i < kCPT; ++i) {
+        const int c = i * bd + tid;
+        const bool active = c < nch;
+        int e;
+        float sval;
+        const uint4 qv = quant_chunk<GSZ, FMT>(v[i][0], v[i][1], e, sval);
+        if (active)
+          for (int k = 0; k < p.K; ++k)
+            if (rows[k] >= 0) st_v4(p.xq + (int64_t)rows[k] * H + c * 16, qv);
+        const int cw = i * bd + (tid & ~31);  // first chunk of this warp
+        if (cw < nch)
+          store_scales<GSZ, FMT>(p, p.K, rows, exps, lane, active, e, sval, cw * 16 / GSZ, G, G4);
+      }
+#pragma unroll
+      for (int i = 0; i < kCPT; ++i) {
+        v[i][0] = vn[i][0];
+        v[i][1] = vn[i][1];
+      }
+    }
+    nlist = 0;  // nothing left for the staged loop below
   }
 
   // ---- token loop ---------------------------------------------------------
@@ -532,9 +579,14 @@ cudaError_t launch_one(const ScatterArgs& a0, int num_sms, bool pdl, cudaStream_
   // The staging ring and the early tokens shrink (down to two buffers and
   // none) until one CTA fits the shared-memory budget.
   ScatterArgs a = a0;
+  a.direct = 0;
+  if (a.mode != kModeIdentity) {
+    if (MOEPERM_SCATTER_DIRECT >= 0) a.direct = MOEPERM_SCATTER_DIRECT;
+    else a.direct = (int64_t)a.K * a.L <= (int64_t)MOEPERM_SCATTER_DIRECT_FANOUT * a.E ? 1 : 0;
+  }
   auto fit = [&](int64_t ntok) {
-    a.stages = kStages;
-    a.pre = (a.mode == kModeIdentity) ? 0 : kPre;
+    a.stages = a.direct ? 0 : kStages;
+    a.pre = (a.mode == kModeIdentity || a.direct) ? 0 : kPre;
     while (smem_bytes(a, ntok, bd) > budget && (a.pre > 0 || a.stages > 2)) {
       if (a.pre > 0) --a.pre; else --a.stages;
     }
