@@ -12,8 +12,9 @@
 // Design: a fixed worker pool (grid = SMs x resident CTAs, capped by R) walks
 // the R expanded rows, one row per warp, so the launch never depends on the
 // routing; a warp finds its row's expert by binary search over the segment
-// starts held in shared memory and copies the row with 16-byte vectors, up to
-// 16 per lane issued before the first store (a 7 KB e4m3 row in one pass). Scales follow each side's own layout (stride
+// starts held in shared memory and copies the row with 16-byte vectors, 8 per
+// lane issued before the first store of each pass (a 7 KB e4m3 row in two
+// passes), at 64 registers so that 3+ CTAs fit per SM. Scales follow each side's own layout (stride
 // aware): row-major bytes / floats, or column-major packed UE8M0 words with
 // one block per expert on the slab side; pad bytes of the last packed word are
 // cleared.
@@ -24,10 +25,16 @@ namespace moeperm {
 
 namespace {
 
+#ifndef MOEPERM_REPACK_PASS
+#define MOEPERM_REPACK_PASS 8
+#endif
+#ifndef MOEPERM_REPACK_MIN_BLOCKS
+#define MOEPERM_REPACK_MIN_BLOCKS 3
+#endif
 constexpr int kThreads = 256;
-constexpr int kPass = 16;   // 16-byte chunks per lane in flight
+constexpr int kPass = MOEPERM_REPACK_PASS;   // 16-byte chunks per lane in flight
 
-__global__ void __launch_bounds__(kThreads) repack_kernel(RepackArgs p) {
+__global__ void __launch_bounds__(kThreads, MOEPERM_REPACK_MIN_BLOCKS) repack_kernel(RepackArgs p) {
   extern __shared__ int32_t sm[];
   int32_t* s_start = sm;
   int32_t* s_psum = sm + p.L;

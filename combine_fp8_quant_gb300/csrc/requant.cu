@@ -11,8 +11,8 @@
 //   q_out[t, h] = RNE_e4m3( fl32( decode(q[t, h]) * fl32(s[t] / S) ) )
 //
 // Design: the max-scale mode is one launch. Rows go one per warp; each warp
-// first issues all the loads of its first row (up to 16 x 16 bytes per lane),
-// then its CTA reduces the T scales (float4 / byte loads, L2-resident) while
+// first issues the loads of the first pass of its first row (8 x 16 bytes per
+// lane), then its CTA reduces the T scales (float4 / byte loads, L2-resident) while
 // they are in flight, and the warp converts and stores: 16 e4m3 bytes per lane
 // per vector, widened exactly with cvt.rn.f16x2.e4m3x2, scaled in fp32,
 // narrowed with cvt.rn.satfinite.e4m3x2.f32. The amax mode adds a first launch
@@ -84,9 +84,16 @@ __device__ __forceinline__ float reduce_e8m0(const uint8_t* b, int n, float* s_r
   return block_max(m ? e8m0_value(m) : 0.0f, s_red);
 }
 
-// Rows are processed one per warp: a lane issues up to kPass 16-byte loads of
-// its row before the first conversion, so a 7 KB row is fully in flight.
-constexpr int kPass = 16;
+// Rows are processed one per warp: a lane issues kPass 16-byte loads of its
+// row before the first conversion of each pass (8: a 7 KB row in two passes,
+// within 80 registers so that 3 CTAs fit per SM).
+#ifndef MOEPERM_REQUANT_PASS
+#define MOEPERM_REQUANT_PASS 8
+#endif
+#ifndef MOEPERM_REQUANT_MIN_BLOCKS
+#define MOEPERM_REQUANT_MIN_BLOCKS 3
+#endif
+constexpr int kPass = MOEPERM_REQUANT_PASS;
 
 // amax mode, launch 1: ws[t] = fl32(s[t] * max_h |decode(q[t, h])|)
 template <int SFMT>
@@ -118,7 +125,7 @@ __global__ void __launch_bounds__(kThreads) requant_rowmax_kernel(RequantArgs p)
 }
 
 template <int SFMT, int MODE>
-__global__ void __launch_bounds__(kThreads) requant_kernel(RequantArgs p) {
+__global__ void __launch_bounds__(kThreads, MOEPERM_REQUANT_MIN_BLOCKS) requant_kernel(RequantArgs p) {
   __shared__ float s_red[kThreads / 32];
   const int lane = threadIdx.x & 31, tid = threadIdx.x;
   const int gwarp = (int)((blockIdx.x * kThreads + threadIdx.x) >> 5);
