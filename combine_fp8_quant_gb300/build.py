@@ -2,7 +2,7 @@
 
 Each translation unit is compiled in parallel to an object file, then linked
 into one shared library with the CUDA runtime linked statically, so the
-library only needs the driver at run time. Register / spill reports from
+library only needs the NVIDIA driver (libcuda) at run time. Register / spill reports from
 ptxas (-Xptxas -v) are written to _build/ptxas_<unit>.log.
 """
 from __future__ import annotations
