@@ -744,10 +744,10 @@ def test_graph_capture_replay_new_routing(dev, ref):
 
 def test_graph_capture_scatter_above_48k_shared_memory(dev, ref):
     """Capture of a two-launch dispatch whose scatter CTA needs more than the
-    default 48 KiB of shared memory (1024 experts: a 36 KiB chunk table), so
-    the launch opts in while the stream is being captured; replays with new
-    routing must match the oracle."""
-    T, H, K, E, L, b, g = 1100, 4096, 2, 1024, 1024, 128, 128
+    default 48 KiB of shared memory (1024 experts, 15 chunks: a 60 KiB chunk
+    table, staged path since K*L/E = 4), so the launch opts in while the stream
+    is being captured; replays with new routing must match the oracle."""
+    T, H, K, E, L, b, g = 900, 4096, 4, 1024, 1024, 16, 128
     rng = np.random.default_rng(41)
     x = bf16_dev(synth.normal_bf16(rng, (T, H)))
     ids = to_dev(synth.uniform_topk(rng, T, E, K))
