@@ -872,12 +872,13 @@ def test_dispatch_max_assignments(dev, ref):
     compact_both(dev, ref, x, ids, w, H, K, L + 2, L, 128, 128, "packed", with_rw=False)
 
 
-@pytest.mark.parametrize("T", [9, 1100])     # 18 slots: one launch; 2200: two launches
-def test_dispatch_max_hidden(dev, ref, T):
+@pytest.mark.parametrize("T,K", [(9, 2), (1100, 2), (1100, 4)])  # one launch; two launches,
+def test_dispatch_max_hidden(dev, ref, T, K):                       # direct (K*L/E = 2) or staged (4)
     """H = 32768: the two-launch scatter covers the row with 1024 threads x 2
-    chunks of 16 in one pass; the one-launch path loops four passes."""
-    rng = np.random.default_rng(21)
-    K, L, H = 2, 8, 32768
+    chunks of 16 in one pass (staged: four 32 KiB staging buffers); the
+    one-launch path loops four passes."""
+    rng = np.random.default_rng(21 + K)
+    L, H = 8, 32768
     x = synth.normal_bf16(rng, (T, H), outlier_frac=0.01)
     ids = synth.uniform_topk(rng, T, L, K)
     w = synth.softmax_weights(rng, T, K)
