@@ -80,6 +80,11 @@ namespace {
 #ifndef MOEPERM_SCATTER_ST_HINT
 #define MOEPERM_SCATTER_ST_HINT 1
 #endif
+// Tokens after the early-staged ones whose x rows are bulk-prefetched into L2
+// before the wait on the route plan (staged path; 0: none).
+#ifndef MOEPERM_SCATTER_PREFETCH_EARLY
+#define MOEPERM_SCATTER_PREFETCH_EARLY 2
+#endif
 // Direct stores instead of staging when few slots per token are kept: 1 =
 // always, 0 = never, -1 = when the expected kept slots per token, K * L / E
 // (uniform routing), are at most MOEPERM_SCATTER_DIRECT_FANOUT.
@@ -321,6 +326,11 @@ __global__ void __launch_bounds__(1024, MOEPERM_SCATTER_MIN_BLOCKS) quant_scatte
     // route plan still runs (their rows are not known yet); their scales wait
     // in shared memory.
     npre = p.direct ? 0 : (ntok < p.pre ? ntok : p.pre);
+    if (MOEPERM_SCATTER_PREFETCH_EARLY > 0 && !p.direct && tid == 0) {
+      const uint64_t pol = l2_policy_evict_last();
+      for (int j = npre; j < ntok && j < npre + MOEPERM_SCATTER_PREFETCH_EARLY; ++j)
+        bulk_prefetch_l2_hint(p.x + (int64_t)(blockIdx.x + j * gridDim.x) * p.ldx, (uint32_t)(2 * H), pol);
+    }
     for (int j = 0; j < npre; ++j) {
       uint4 vn[kCPT][2];
       load_row(vn, j + 1 < npre ? p.x + (int64_t)(blockIdx.x + (j + 1) * gridDim.x) * p.ldx : nullptr,
