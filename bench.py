@@ -811,6 +811,72 @@ def layout_sweep(args):
             del xq, sc, mi, xqm, scm
 
 
+def shape_sweep(args):
+    """The dispatch + combine step on other MoE shapes (hidden size, experts,
+    top-k, tokens), all experts local, Zipf(1.2) routing with 12 empty experts
+    where there are enough experts, group-128 packed UE8M0 scales, block_e
+    128. Each call and the whole step are timed as CUDA-graph replays after
+    an L2 flush (trimmed mean of 40). One JSON line per shape."""
+    import torch
+    import combine_fp8_quant_gb300 as mp
+    from combine_fp8_quant_gb300 import build as cuda_build
+    cuda_build.build()
+    mp.load()
+    dev = torch.device("cuda:0")
+    flush = L2Flush(dev)
+    hbm, _ = peaks()
+    g, b = 128, 128
+    for T, H, E, K in ((8192, 7168, 256, 8), (32768, 7168, 256, 8), (8192, 4096, 128, 8),
+                       (8192, 5120, 160, 6), (16384, 2048, 64, 6), (4096, 7168, 256, 8)):
+        L = E
+        rng = np.random.default_rng(T + H + E + K)
+        x = torch.from_numpy(synth.normal_bf16(rng, (T, H)).view(np.int16)).to(dev).view(torch.bfloat16)
+        ids_np = synth.zipf_topk(rng, T, E, K, n_empty=min(12, E - K))
+        ids = torch.from_numpy(ids_np).to(dev)
+        w = torch.from_numpy(synth.softmax_weights(rng, T, K)).to(dev)
+        kept = int(((ids_np >= 0) & (ids_np < L)).sum())
+        db, cbytes = dispatch_bytes(T, H, K, L, b, g, kept), combine_bytes(T, H, K, kept)
+        ws = mp.Workspace(T, K, L, dev)
+        st = torch.zeros(1, dtype=torch.int32, device=dev)
+        bound = mp.moe_compact_bound(T * K, L, b)
+        xq = torch.empty((bound, H), dtype=torch.uint8, device=dev)
+        sc, ld = mp.scale_tensor("packed", bound, H, g, dev)
+        mi = torch.empty(bound, dtype=torch.int32, device=dev)
+        s2d = torch.empty((T, K), dtype=torch.int32, device=dev)
+        c3 = [torch.empty(L, dtype=torch.int32, device=dev) for _ in range(3)]
+        tot = torch.empty(1, dtype=torch.int32, device=dev)
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(T)
+        y = torch.randn((bound, H), generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+
+        def disp():
+            assert mp.moe_dispatch_compact(x, H, T, None, H, ids, None, K, E, L, b, g, "packed", xq, sc,
+                                           ld, mi, bound, s2d, *c3, tot, None, ws.buf, ws.nbytes, st) == 0
+
+        def comb():
+            assert mp.moe_combine(y, H, bound, s2d, w, T, None, K, H, out, st) == 0
+        disp()
+        comb()
+        torch.cuda.synchronize()
+        graphs = {}
+        for name, fns in (("step", (disp, comb)), ("dispatch", (disp,)), ("combine", (comb,))):
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr):
+                for fn in fns:
+                    fn()
+            graphs[name] = gr
+        us = {name: time_call(gr.replay, flush) for name, gr in graphs.items()}
+        torch.cuda.synchronize()
+        assert mp.moe_status_sync(st) == 0
+        line = {"shape_sweep": True, "T": T, "H": H, "E": E, "K": K, "kept_slots": kept}
+        for name, nbytes in (("step", db + cbytes), ("dispatch", db), ("combine", cbytes)):
+            gbs = nbytes / (us[name] * 1e-6) / 1e9
+            line[name] = {"us": us[name], "gbs": gbs, "frac_of_peak": gbs / hbm}
+        print(json.dumps(line), flush=True)
+        del graphs, y, xq, x
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -824,9 +890,14 @@ def main():
                     help="override T of the prefill workload (profiling smaller cases)")
     ap.add_argument("--layout-sweep", action="store_true",
                     help="compact vs masked dispatch cost over (T, L); one JSON line per point")
+    ap.add_argument("--shape-sweep", action="store_true",
+                    help="the dispatch + combine step on other (T, H, E, K) shapes; one JSON line per shape")
     args = ap.parse_args()
     if args.layout_sweep:
         layout_sweep(args)
+        return
+    if args.shape_sweep:
+        shape_sweep(args)
         return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
