@@ -45,12 +45,6 @@ bool ld_ok(int fmt, int64_t ld, int64_t rows_per_block, int G) {
   return ld >= G;
 }
 
-int64_t route_nchunks(int64_t A, int S) {
-  const int64_t per = kRouteThreads * (int64_t)S;
-  int64_t n = (A + per - 1) / per;
-  return n < 1 ? 1 : n;
-}
-
 moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 struct DispatchCommon {
@@ -65,7 +59,7 @@ moe_status_t check_common(const DispatchCommon& c) {
   if (!fmt_ok(c.fmt, c.g)) return MOE_ERR_INVALID_ARG;
   if (c.K < 1 || c.K > kMaxK || c.L < 1 || c.L > kMaxL || c.E < c.L) return MOE_ERR_INVALID_ARG;
   if ((int64_t)c.T * c.K > kMaxAssignments || c.H > kMaxHidden) return MOE_ERR_INVALID_ARG;
-  if (route_plan_S((int64_t)c.T * c.K, c.L) == 0) return MOE_ERR_INVALID_ARG;
+  if (route_geometry((int64_t)c.T * c.K, c.L, route_table_pref(c.H)).S == 0) return MOE_ERR_INVALID_ARG;
   if (c.T > 0) {
     if (!c.x || !aligned16(c.x) || c.ldx < c.H || c.ldx % 8) return MOE_ERR_INVALID_ARG;
     if (!c.ids || !c.src2dst) return MOE_ERR_INVALID_ARG;
@@ -95,16 +89,15 @@ moe_status_t run_dispatch(const DispatchCommon& c, int mode, int32_t block_e, in
     sa.masked_m = masked_m; sa.status = d_status;
     return cuda_status(launch_dispatch_small(sa, c.g, c.fmt, sms, stream));
   }
-  const int S = route_plan_S(A, c.L);
-  const int64_t nchunks = route_nchunks(A, S);
+  const RouteGeom geom = route_geometry(A, c.L, route_table_pref(c.H));
   int32_t* table = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(c.ws) + kWsHeader);
 
   RoutePlanArgs rp{};
   rp.ids = c.ids; rp.d_num_tokens = c.d_num_tokens;
   rp.T = c.T; rp.K = c.K; rp.L = c.L;
-  rp.chunk = kRouteThreads * S; rp.nchunks = (int32_t)nchunks;
+  rp.chunk = geom.chunk; rp.nchunks = (int32_t)geom.nchunks;
   rp.lrank = c.src2dst; rp.table = table; rp.status = d_status;
-  if (launch_route_plan(rp, S, stream) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_route_plan(rp, geom, stream) != cudaSuccess) return MOE_ERR_CUDA;
 
   ScatterArgs sa{};
   sa.x = static_cast<const uint16_t*>(c.x); sa.ldx = c.ldx; sa.T = c.T;
@@ -142,10 +135,16 @@ size_t moe_scale_bytes(moe_scale_fmt_t fmt, int64_t rows, int32_t H, int32_t g) 
 size_t moe_workspace_bytes(int32_t T, int32_t K, int32_t L) {
   if (T < 0 || K < 1 || L < 1) return 0;
   const int64_t A = (int64_t)T * K;
-  const int S = route_plan_S(A, L);
-  if (S == 0) return 0;
-  const int64_t nchunks = route_nchunks(A, S);
-  return kWsHeader + (size_t)nchunks * (size_t)L * sizeof(int32_t);
+  // the larger table of the two row-width preferences, so one workspace fits
+  // every H (a preference that no chain meets falls back to the shortest
+  // chain under the hard limit, which can be the larger table)
+  int64_t nc = 0;
+  for (int64_t pref : {route_table_pref(kNarrowRow - 16), route_table_pref(kNarrowRow)}) {
+    const RouteGeom geom = route_geometry(A, L, pref);
+    if (geom.S == 0) return 0;
+    if (geom.nchunks > nc) nc = geom.nchunks;
+  }
+  return kWsHeader + (size_t)nc * (size_t)L * sizeof(int32_t);
 }
 
 moe_status_t moe_dispatch_compact(

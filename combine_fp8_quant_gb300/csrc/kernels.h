@@ -15,23 +15,41 @@ constexpr int kMaxTableInts = 16384;
 // ---------------------------------------------------------------------------
 // Route plan: per-chunk expert histograms and stable in-chunk ranks.
 // ---------------------------------------------------------------------------
-#ifndef MOEPERM_ROUTE_WARPS
-#define MOEPERM_ROUTE_WARPS 8
-#endif
-constexpr int kRouteWarps = MOEPERM_ROUTE_WARPS;
-constexpr int kRouteThreads = 32 * kRouteWarps;   // a chunk holds kRouteThreads * S slots
 struct RoutePlanArgs {
   const int32_t* ids;          // [T, K]
   const int32_t* d_num_tokens; // optional live tokens
   int32_t T, K, L;
-  int32_t chunk;               // assignments per chunk (= 256 * S)
+  int32_t chunk;               // assignments per chunk (= 32 * warps * S)
   int32_t nchunks;
   int32_t* lrank;              // [T*K] out: stable rank inside the chunk, -1 dropped
   int32_t* table;              // [nchunks, L] out: chunk histogram
   int32_t* status;
 };
-int route_plan_S(int64_t A, int L);                 // 0 if the table cannot fit
-cudaError_t launch_route_plan(const RoutePlanArgs& a, int S, cudaStream_t s);
+// Launch geometry of the route plan: S slots per lane (the length of each
+// warp's dependent chain), warps per CTA, chunk = 32 * warps * S slots per CTA.
+struct RouteGeom {
+  int S;                       // 0: the chunk table cannot fit kMaxTableInts
+  int warps;
+  int32_t chunk;
+  int64_t nchunks;
+};
+// The shortest chain S whose table (chunks x L) fits table_pref ints, else
+// the shortest whose table fits kMaxTableInts. A smaller table costs a longer
+// chain but less shared memory and fewer table loads in every scatter CTA;
+// narrow rows (many small scatter CTAs per SM, each loading the table) prefer
+// the smaller one. Measured on GB300 across T, H, E, top-k shapes.
+#ifndef MOEPERM_ROUTE_TABLE_PREF
+#define MOEPERM_ROUTE_TABLE_PREF 8192
+#endif
+#ifndef MOEPERM_ROUTE_TABLE_PREF_NARROW
+#define MOEPERM_ROUTE_TABLE_PREF_NARROW 2048
+#endif
+constexpr int kNarrowRow = 4096;   // H below this: the narrow-row preference
+inline int64_t route_table_pref(int H) {
+  return H < kNarrowRow ? MOEPERM_ROUTE_TABLE_PREF_NARROW : MOEPERM_ROUTE_TABLE_PREF;
+}
+RouteGeom route_geometry(int64_t A, int L, int64_t table_pref);
+cudaError_t launch_route_plan(const RoutePlanArgs& a, const RouteGeom& g, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
 // Quantise + scatter (dispatch) / quantise live rows (identity mode).

@@ -9,16 +9,20 @@
 // The prefix sums over chunks and experts (segment starts, psum, total,
 // masked_m) are formed from this table by every CTA of the scatter launch.
 //
-// Design (fixed grid of `nchunks` CTAs of kRouteWarps warps): CTA c owns slots
-// [c*chunk, (c+1)*chunk); warp w owns a contiguous sub-range of 32*S of them,
-// walked in order in steps of 32. In a step, ballots over the bits of the
-// expert id group the lanes with the same expert; a lane's rank among them is
-// the popcount of its lower peers, and the lowest peer adds the group size to
-// the warp's per-expert counter in shared memory. A per-expert scan over the
-// warps turns the warp-local ranks into chunk-local ones. Deterministic and stable, with no
-// global atomics. The CTA signals the dependent scatter launch at its start,
-// so that launch is scheduled while this one runs (it waits for this grid's
-// results before reading them).
+// Design (grid of `nchunks` CTAs of W warps each, both chosen per launch by
+// route_geometry): CTA c owns slots [c*chunk, (c+1)*chunk); warp w owns a
+// contiguous sub-range of 32*S of them, walked in order in steps of 32. In a
+// step, the lanes with the same expert are grouped (one match instruction, or
+// one ballot per bit of the expert id); a lane's rank among them is the
+// popcount of its lower peers, and the lowest peer adds the group size to the
+// warp's per-expert counter in shared memory. A per-expert scan over the
+// warps turns the warp-local ranks into chunk-local ones. Deterministic and
+// stable, with no global atomics. The steps of one warp form a dependent
+// chain, so the launch keeps S (the chain length) short and puts up to 32
+// warps in a CTA instead: the chunk size, and so the table the scatter launch
+// scans, stays small without a long chain. The CTA signals the dependent
+// scatter launch at its start, so that launch is scheduled while this one
+// runs (it waits for this grid's results before reading them).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -26,21 +30,26 @@ namespace moeperm {
 
 namespace {
 
-constexpr int kWarps = kRouteWarps;
-constexpr int kThreads = kRouteThreads;
 constexpr int kGroup = 8;  // steps whose peer masks are formed together
-#ifndef MOEPERM_ROUTE_MAX_CHUNKS
-#define MOEPERM_ROUTE_MAX_CHUNKS 16
+// Peer masks from __match_any_sync (1) or from one ballot per expert-id bit (0).
+#ifndef MOEPERM_ROUTE_MATCH
+#define MOEPERM_ROUTE_MATCH 1
 #endif
+// Per-warp histograms (warps x local experts, int32) a CTA may hold: 48 KiB.
+constexpr int kHistInts = 12288;
+// Warps a CTA may have for chain length S: the S = 64 kernel keeps its 64
+// expert ids in registers and is built for 256 threads.
+constexpr int max_warps_for(int S) { return S > 16 ? 8 : 32; }
 
 template <int S>
-__global__ void __launch_bounds__(kThreads) route_plan_kernel(RoutePlanArgs p) {
-  extern __shared__ int32_t smem[];  // [kWarps][L] per-warp histograms
+__global__ void __launch_bounds__(32 * max_warps_for(S)) route_plan_kernel(RoutePlanArgs p) {
+  extern __shared__ int32_t smem[];  // [warps][L] per-warp histograms
   pdl_launch_dependents();
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, bd = blockDim.x;
+  const int nw = bd >> 5;
   const int L = p.L;
 
-  for (int i = tid; i < kWarps * L; i += kThreads) smem[i] = 0;
+  for (int i = tid; i < nw * L; i += bd) smem[i] = 0;
   const int n_live = live_count(p.d_num_tokens, p.T, p.status, blockIdx.x == 0 && tid == 0);
   const int64_t A = (int64_t)p.T * p.K;
   const int64_t A_live = (int64_t)n_live * p.K;
@@ -53,10 +62,11 @@ __global__ void __launch_bounds__(kThreads) route_plan_kernel(RoutePlanArgs p) {
   }
   __syncthreads();
 
-  // Lanes with the same expert ("peers") are found with one ballot per bit of
-  // the expert id: a lane keeps the lanes that agree with it on every bit.
-  // The masks of 8 steps are formed first (independent), then the per-warp
-  // counters are advanced step by step in order, which fixes a stable rank.
+  // Lanes with the same expert ("peers"): one match over the warp, or one
+  // ballot per bit of the expert id (a lane keeps the lanes that agree with it
+  // on every bit). The masks of 8 steps are formed first (independent), then
+  // the per-warp counters are advanced step by step in order, which fixes a
+  // stable rank.
   int32_t* myhw = smem + warp * L;
   const unsigned lt_mask = (1u << lane) - 1u;
   const int nbits = (L > 1) ? 32 - __clz(L - 1) : 0;
@@ -69,11 +79,16 @@ __global__ void __launch_bounds__(kThreads) route_plan_kernel(RoutePlanArgs p) {
       int e = v[i0 + j];
       if (e < 0 || e >= L) e = -1;
       v[i0 + j] = e;
-      unsigned m = __ballot_sync(0xffffffffu, e >= 0);
-      for (int b = 0; b < nbits; ++b) {
-        const unsigned bit = (unsigned)(e >> b) & 1u;
-        const unsigned bal = __ballot_sync(0xffffffffu, bit);
-        m &= bit ? bal : ~bal;
+      unsigned m;
+      if (MOEPERM_ROUTE_MATCH) {
+        m = __match_any_sync(0xffffffffu, e);
+      } else {
+        m = __ballot_sync(0xffffffffu, e >= 0);
+        for (int b = 0; b < nbits; ++b) {
+          const unsigned bit = (unsigned)(e >> b) & 1u;
+          const unsigned bal = __ballot_sync(0xffffffffu, bit);
+          m &= bit ? bal : ~bal;
+        }
       }
       peers[j] = (e >= 0) ? m : 0u;
     }
@@ -92,11 +107,21 @@ __global__ void __launch_bounds__(kThreads) route_plan_kernel(RoutePlanArgs p) {
   }
   __syncthreads();
 
-  // per-expert exclusive scan over the warps; chunk histogram to the table
-  for (int e = tid; e < L; e += kThreads) {
-    int run = 0;
+  // per-expert exclusive scan over the warps (8 loads in flight, then 8
+  // stores); chunk histogram to the table
+  for (int e = tid; e < L; e += bd) {
+    int run = 0, w = 0;
+    for (; w + 8 <= nw; w += 8) {
+      int h[8];
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
+      for (int j = 0; j < 8; ++j) h[j] = smem[(w + j) * L + e];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        smem[(w + j) * L + e] = run;
+        run += h[j];
+      }
+    }
+    for (; w < nw; ++w) {
       const int c = smem[w * L + e];
       smem[w * L + e] = run;
       run += c;
@@ -116,31 +141,43 @@ __global__ void __launch_bounds__(kThreads) route_plan_kernel(RoutePlanArgs p) {
 
 }  // namespace
 
-int route_plan_S(int64_t A, int L) {
-  // Smallest S whose chunk table fits kMaxTableInts (the scatter launch holds
-  // it in shared memory), preferring at most 16 chunks (a smaller table for
-  // every scatter CTA to scan).
-  const int cand[] = {1, 4, 16, 64};
-  for (int S : cand) {
-    const int64_t nc = (A + (int64_t)kThreads * S - 1) / ((int64_t)kThreads * S);
-    if (nc <= MOEPERM_ROUTE_MAX_CHUNKS && nc * L <= kMaxTableInts) return S;
+RouteGeom route_geometry(int64_t A, int L, int64_t table_pref) {
+  RouteGeom g{};
+  if (L < 1) return g;
+  const int wmax = L >= kHistInts ? 1 : (kHistInts / L < 32 ? kHistInts / L : 32);
+  const int cand[] = {1, 2, 4, 8, 16, 64};
+  for (int64_t limit : {table_pref, (int64_t)kMaxTableInts}) {
+    for (int S : cand) {
+      const int W = wmax < max_warps_for(S) ? wmax : max_warps_for(S);
+      const int64_t chunk = (int64_t)32 * W * S;
+      int64_t nc = (A + chunk - 1) / chunk;
+      if (nc < 1) nc = 1;
+      if (nc * L <= limit) {
+        g.S = S;
+        g.warps = W;
+        g.chunk = (int32_t)chunk;
+        g.nchunks = nc;
+        return g;
+      }
+    }
   }
-  for (int S : cand) {
-    const int64_t nc = (A + (int64_t)kThreads * S - 1) / ((int64_t)kThreads * S);
-    if (nc * L <= kMaxTableInts) return S;
-  }
-  return 0;  // too large for one call
+  return g;  // S == 0: too large for one call
 }
 
-cudaError_t launch_route_plan(const RoutePlanArgs& a, int S, cudaStream_t s) {
-  const size_t smem = (size_t)kWarps * a.L * sizeof(int32_t);
-  dim3 grid(a.nchunks), block(kThreads);
-  switch (S) {
-    case 1: route_plan_kernel<1><<<grid, block, smem, s>>>(a); break;
-    case 4: route_plan_kernel<4><<<grid, block, smem, s>>>(a); break;
-    case 16: route_plan_kernel<16><<<grid, block, smem, s>>>(a); break;
-    default: route_plan_kernel<64><<<grid, block, smem, s>>>(a); break;
+cudaError_t launch_route_plan(const RoutePlanArgs& a, const RouteGeom& g, cudaStream_t s) {
+  const size_t smem = (size_t)g.warps * a.L * sizeof(int32_t);
+  dim3 grid((unsigned)a.nchunks), block(32 * g.warps);
+  cudaError_t err = cudaSuccess;
+  switch (g.S) {
+    case 1: err = opt_in_smem(route_plan_kernel<1>, smem); if (!err) route_plan_kernel<1><<<grid, block, smem, s>>>(a); break;
+    case 2: err = opt_in_smem(route_plan_kernel<2>, smem); if (!err) route_plan_kernel<2><<<grid, block, smem, s>>>(a); break;
+    case 4: err = opt_in_smem(route_plan_kernel<4>, smem); if (!err) route_plan_kernel<4><<<grid, block, smem, s>>>(a); break;
+    case 8: err = opt_in_smem(route_plan_kernel<8>, smem); if (!err) route_plan_kernel<8><<<grid, block, smem, s>>>(a); break;
+    case 16: err = opt_in_smem(route_plan_kernel<16>, smem); if (!err) route_plan_kernel<16><<<grid, block, smem, s>>>(a); break;
+    case 64: err = opt_in_smem(route_plan_kernel<64>, smem); if (!err) route_plan_kernel<64><<<grid, block, smem, s>>>(a); break;
+    default: return cudaErrorInvalidValue;
   }
+  if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
 

@@ -861,15 +861,29 @@ def test_prefill_full_size_sampled(dev, ref):
 # ---------------------------------------------------------------------------
 
 def test_dispatch_max_assignments(dev, ref):
-    """T*K = 2^20 slots (the largest accepted): 256 route-plan chunks of 4096
-    slots x 64 experts, a full 64 KiB chunk table."""
+    """T*K = 2^20 slots (the largest accepted) over 256 experts: 64 route-plan
+    chunks of 16384 slots (32 warps x 16 steps), a full 64 KiB chunk table."""
     rng = np.random.default_rng(20)
-    T, K, L, H = 131072, 8, 64, 128
+    T, K, L, H = 131072, 8, 256, 128
     x = synth.normal_bf16(rng, (T, H))
     ids = rng.integers(-1, L + 2, size=(T, K)).astype(np.int32)   # a few dropped slots
     w = rng.random((T, K)).astype(np.float32)
     assert dev.moe_workspace_bytes(T, K, L) == 256 + 16384 * 4
     compact_both(dev, ref, x, ids, w, H, K, L + 2, L, 128, 128, "packed", with_rw=False)
+
+
+def test_dispatch_long_route_chain(dev, ref):
+    """1024 local experts x 262144 slots: only 8 warps fit the per-warp
+    histograms, so each lane walks 64 slots (16 chunks of 16384, a full
+    64 KiB table)."""
+    rng = np.random.default_rng(23)
+    T, K, L, H = 8192, 32, 1024, 128
+    x = synth.normal_bf16(rng, (T, H))
+    ids = synth.zipf_topk(rng, T, L, K, n_empty=24)
+    w = synth.softmax_weights(rng, T, K)
+    assert dev.moe_workspace_bytes(T, K, L) == 256 + 16384 * 4
+    compact_both(dev, ref, x, ids, w, H, K, L, L, 128, 128, "packed")
+    masked_both(dev, ref, x, ids, w, H, K, L, L, 256, 128, "packed")
 
 
 @pytest.mark.parametrize("T,K", [(9, 2), (1100, 2), (1100, 4)])  # one launch; two launches,
