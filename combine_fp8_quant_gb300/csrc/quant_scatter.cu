@@ -25,7 +25,8 @@
 // Design: a persistent grid (SMs x resident CTAs, independent of the routing)
 // walks the live tokens, t = blockIdx.x + i * gridDim.x. One thread owns two
 // 16-element chunks of a row (two 16-byte loads each), so a single pass
-// covers H <= 32768.
+// covers H <= 32768; rows up to 5120 elements take one chunk per thread
+// instead, so that their CTAs keep enough threads (and loads) in flight.
 //   Prologue: this grid is already resident while the route plan runs
 //   (programmatic dependent launch), so before waiting for it a CTA reads and
 //   quantises its first few tokens into their staging buffers (inputs only:
@@ -62,9 +63,12 @@ namespace {
 #ifndef MOEPERM_SCATTER_PRE
 #define MOEPERM_SCATTER_PRE 2
 #endif
-#ifndef MOEPERM_SCATTER_CPT
-#define MOEPERM_SCATTER_CPT 2
+// Rows up to this width take one 16-element chunk per thread (twice the
+// threads per CTA); wider rows take two.
+#ifndef MOEPERM_SCATTER_CPT1_MAX_H
+#define MOEPERM_SCATTER_CPT1_MAX_H 5120
 #endif
+static_assert(MOEPERM_SCATTER_CPT1_MAX_H <= 16384, "one chunk per thread covers at most 1024 x 16 elements");
 #ifndef MOEPERM_SCATTER_MIN_BLOCKS
 #define MOEPERM_SCATTER_MIN_BLOCKS 1
 #endif
@@ -94,7 +98,6 @@ namespace {
 #ifndef MOEPERM_SCATTER_DIRECT_FANOUT
 #define MOEPERM_SCATTER_DIRECT_FANOUT 3
 #endif
-constexpr int kCPT = MOEPERM_SCATTER_CPT;          // 16-element chunks per thread
 // Largest staging ring (rows in flight to the bulk-copy engine) and number of
 // tokens quantised before the wait on the route plan; the launch lowers both
 // when shared memory is short (large H with a large chunk table).
@@ -105,7 +108,7 @@ static_assert(kStages >= 2 && kStages <= 6, "staging ring of 2 to 6 rows");
 // Dynamic shared memory: [table nchunks*L | starts L | psum L | rows ntok*K |
 // experts ntok*K | token list ntok] (dispatch modes only), then, at a 128-byte boundary,
 // p.stages staged rows of H bytes and the scales of the tokens staged early
-// (p.pre x kCPT x threads words).
+// (p.pre x CPT x threads words, CPT = 16-element chunks per thread).
 __host__ __device__ inline size_t layout_bytes(const ScatterArgs& p, int64_t ntok) {
   if (p.mode == kModeIdentity) return 0;
   return ((size_t)p.nchunks * p.L + 2 * (size_t)p.L + 2 * (size_t)ntok * p.K + (size_t)ntok) *
@@ -114,10 +117,10 @@ __host__ __device__ inline size_t layout_bytes(const ScatterArgs& p, int64_t nto
 __host__ __device__ inline size_t stage_offset(const ScatterArgs& p, int64_t ntok) {
   return (layout_bytes(p, ntok) + 127) / 128 * 128;
 }
-__host__ __device__ inline size_t smem_bytes(const ScatterArgs& p, int64_t ntok, int bd) {
+__host__ __device__ inline size_t smem_bytes(const ScatterArgs& p, int64_t ntok, int bd, int cpt) {
   if (p.mode == kModeIdentity) return 0;  // direct stores, nothing staged
   if (p.direct) return stage_offset(p, ntok);
-  return stage_offset(p, ntok) + (size_t)p.stages * p.H + (size_t)p.pre * kCPT * bd * sizeof(int32_t);
+  return stage_offset(p, ntok) + (size_t)p.stages * p.H + (size_t)p.pre * cpt * bd * sizeof(int32_t);
 }
 
 // Wait until at most n - 2 bulk groups of this thread still read shared
@@ -137,10 +140,11 @@ __device__ inline int64_t ntok_smem(const ScatterArgs& p) {
 }
 
 
-__device__ __forceinline__ void load_row(uint4 (&v)[kCPT][2], const uint16_t* xrow, int nch,
+template <int CPT>
+__device__ __forceinline__ void load_row(uint4 (&v)[CPT][2], const uint16_t* xrow, int nch,
                                          int bd, int tid) {
 #pragma unroll
-  for (int i = 0; i < kCPT; ++i) {
+  for (int i = 0; i < CPT; ++i) {
     const int c = i * bd + tid;
     if (xrow != nullptr && c < nch) {
       v[i][0] = ld_nc_v4(xrow + c * 16);
@@ -284,7 +288,7 @@ __device__ __forceinline__ int slot_row(const ScatterArgs& p, const int32_t* tbl
   return j < p.cap ? e * p.cap + j : -1;
 }
 
-template <int GSZ, int FMT>
+template <int GSZ, int FMT, int CPT>
 __global__ void __launch_bounds__(1024, MOEPERM_SCATTER_MIN_BLOCKS) quant_scatter_kernel(ScatterArgs p) {
   extern __shared__ int32_t sm[];
   __shared__ int32_t s_wsum[32];
@@ -307,13 +311,13 @@ __global__ void __launch_bounds__(1024, MOEPERM_SCATTER_MIN_BLOCKS) quant_scatte
 
   // Inputs only, before anything waits: the first token's row and the expert
   // id of this thread's first slot.
-  uint4 v[kCPT][2];
+  uint4 v[CPT][2];
   load_row(v, ntok > 0 ? p.x + (int64_t)blockIdx.x * p.ldx : nullptr, nch, bd, tid);
   const int64_t a0 = tid < nsl ? slot_of(tid) : -1;
   const int e0 = a0 >= 0 ? __ldg(p.ids + a0) : -1;
 
   uint8_t* stage = reinterpret_cast<uint8_t*>(sm) + stage_offset(p, ntok_smem(p));
-  int32_t* pre_s = reinterpret_cast<int32_t*>(stage + (size_t)p.stages * H);  // [pre][kCPT][bd]
+  int32_t* pre_s = reinterpret_cast<int32_t*>(stage + (size_t)p.stages * H);  // [pre][CPT][bd]
   int32_t* rows_s = sm;  // identity mode: unused
   int32_t* exps_s = sm;  // expert of each slot (masked scale blocks)
   int32_t* list_s = sm;  // iteration -> token index of this CTA (dispatch modes)
@@ -332,21 +336,21 @@ __global__ void __launch_bounds__(1024, MOEPERM_SCATTER_MIN_BLOCKS) quant_scatte
         bulk_prefetch_l2_hint(p.x + (int64_t)(blockIdx.x + j * gridDim.x) * p.ldx, (uint32_t)(2 * H), pol);
     }
     for (int j = 0; j < npre; ++j) {
-      uint4 vn[kCPT][2];
+      uint4 vn[CPT][2];
       load_row(vn, j + 1 < npre ? p.x + (int64_t)(blockIdx.x + (j + 1) * gridDim.x) * p.ldx : nullptr,
                nch, bd, tid);
       uint8_t* sb = stage + (size_t)j * H;
 #pragma unroll
-      for (int i = 0; i < kCPT; ++i) {
+      for (int i = 0; i < CPT; ++i) {
         const int c = i * bd + tid;
         int e;
         float sval;
         const uint4 qv = quant_chunk<GSZ, FMT>(v[i][0], v[i][1], e, sval);
         if (c < nch) *reinterpret_cast<uint4*>(sb + c * 16) = qv;
-        pre_s[(j * kCPT + i) * bd + tid] = (FMT == kFmtF32) ? __float_as_int(sval) : e;
+        pre_s[(j * CPT + i) * bd + tid] = (FMT == kFmtF32) ? __float_as_int(sval) : e;
       }
 #pragma unroll
-      for (int i = 0; i < kCPT; ++i) {
+      for (int i = 0; i < CPT; ++i) {
         v[i][0] = vn[i][0];
         v[i][1] = vn[i][1];
       }
@@ -415,11 +419,11 @@ __global__ void __launch_bounds__(1024, MOEPERM_SCATTER_MIN_BLOCKS) quant_scatte
     for (int it = 0; it < ntok; ++it) {
       const int t = blockIdx.x + it * gridDim.x;
       const int tn = t + gridDim.x;
-      uint4 vn[kCPT][2];
+      uint4 vn[CPT][2];
       load_row(vn, tn < n_live ? p.x + (int64_t)tn * p.ldx : nullptr, nch, bd, tid);
       const int rows[1] = {t};
 #pragma unroll
-      for (int i = 0; i < kCPT; ++i) {
+      for (int i = 0; i < CPT; ++i) {
         const int c = i * bd + tid;
         const bool active = c < nch;
         int e;
@@ -430,7 +434,7 @@ __global__ void __launch_bounds__(1024, MOEPERM_SCATTER_MIN_BLOCKS) quant_scatte
         if (cw < nch) store_scales<GSZ, FMT>(p, 1, rows, rows, lane, active, e, sval, cw * 16 / GSZ, G, G4);
       }
 #pragma unroll
-      for (int i = 0; i < kCPT; ++i) {
+      for (int i = 0; i < CPT; ++i) {
         v[i][0] = vn[i][0];
         v[i][1] = vn[i][1];
       }
@@ -444,13 +448,13 @@ __global__ void __launch_bounds__(1024, MOEPERM_SCATTER_MIN_BLOCKS) quant_scatte
     for (int n = 0; n < nlist; ++n) {
       const int it = list_s[n];
       const int itn = n + 1 < nlist ? list_s[n + 1] : -1;
-      uint4 vn[kCPT][2];
+      uint4 vn[CPT][2];
       load_row(vn, itn >= 0 ? p.x + (int64_t)(blockIdx.x + itn * gridDim.x) * p.ldx : nullptr,
                nch, bd, tid);
       const int* rows = rows_s + it * p.K;
       const int* exps = exps_s + it * p.K;
 #pragma unroll
-      for (int i = 0; i < kCPT; ++i) {
+      for (int i = 0; i < CPT; ++i) {
         const int c = i * bd + tid;
         const bool active = c < nch;
         int e;
@@ -464,7 +468,7 @@ __global__ void __launch_bounds__(1024, MOEPERM_SCATTER_MIN_BLOCKS) quant_scatte
           store_scales<GSZ, FMT>(p, p.K, rows, exps, lane, active, e, sval, cw * 16 / GSZ, G, G4);
       }
 #pragma unroll
-      for (int i = 0; i < kCPT; ++i) {
+      for (int i = 0; i < CPT; ++i) {
         v[i][0] = vn[i][0];
         v[i][1] = vn[i][1];
       }
@@ -500,7 +504,7 @@ __global__ void __launch_bounds__(1024, MOEPERM_SCATTER_MIN_BLOCKS) quant_scatte
     const bool staged = n < npre;  // the staged tokens are list entries 0 .. npre-1
     const bool fetch = n + 1 >= npre;
     prefetch_x(n + 1 + MOEPERM_SCATTER_L2PF);
-    uint4 vn[kCPT][2];
+    uint4 vn[CPT][2];
     if (fetch) {
       const int itn = n + 1 < nlist ? (identity ? n + 1 : list_s[n + 1]) : -1;
       load_row(vn, itn >= 0 ? p.x + (int64_t)(blockIdx.x + itn * gridDim.x) * p.ldx : nullptr,
@@ -517,13 +521,13 @@ __global__ void __launch_bounds__(1024, MOEPERM_SCATTER_MIN_BLOCKS) quant_scatte
     const int buf = n % p.stages;
     uint8_t* sb = stage + (size_t)buf * H;
 #pragma unroll
-    for (int i = 0; i < kCPT; ++i) {
+    for (int i = 0; i < CPT; ++i) {
       const int c = i * bd + tid;
       const bool active = c < nch;
       int e;
       float sval;
       if (staged) {
-        const int w = pre_s[(it * kCPT + i) * bd + tid];
+        const int w = pre_s[(it * CPT + i) * bd + tid];
         e = w;
         sval = __int_as_float(w);
       } else {
@@ -550,7 +554,7 @@ __global__ void __launch_bounds__(1024, MOEPERM_SCATTER_MIN_BLOCKS) quant_scatte
     }
     if (fetch) {
 #pragma unroll
-      for (int i = 0; i < kCPT; ++i) {
+      for (int i = 0; i < CPT; ++i) {
         v[i][0] = vn[i][0];
         v[i][1] = vn[i][1];
       }
@@ -573,10 +577,10 @@ __global__ void __launch_bounds__(1024, MOEPERM_SCATTER_MIN_BLOCKS) quant_scatte
   if (tid == 0) bulk_wait_all();
 }
 
-template <int GSZ, int FMT>
+template <int GSZ, int FMT, int CPT>
 cudaError_t launch_one(const ScatterArgs& a0, int num_sms, bool pdl, cudaStream_t s) {
   const int nch = a0.H / 16;
-  int bd = (nch + kCPT - 1) / kCPT;
+  int bd = (nch + CPT - 1) / CPT;
   bd = (bd + 31) / 32 * 32;
   if (bd > 1024) return cudaErrorInvalidValue;  // H > 32768 is rejected on the host
   int dev = 0, optin = 0;
@@ -597,17 +601,17 @@ cudaError_t launch_one(const ScatterArgs& a0, int num_sms, bool pdl, cudaStream_
   auto fit = [&](int64_t ntok) {
     a.stages = a.direct ? 0 : kStages;
     a.pre = (a.mode == kModeIdentity || a.direct) ? 0 : kPre;
-    while (smem_bytes(a, ntok, bd) > budget && (a.pre > 0 || a.stages > 2)) {
+    while (smem_bytes(a, ntok, bd, CPT) > budget && (a.pre > 0 || a.stages > 2)) {
       if (a.pre > 0) --a.pre; else --a.stages;
     }
     if (a.pre > a.stages) a.pre = a.stages;
   };
   fit(16);
   int per_sm = 0;
-  err = opt_in_smem(quant_scatter_kernel<GSZ, FMT>, smem_bytes(a, 16, bd));
+  err = opt_in_smem(quant_scatter_kernel<GSZ, FMT, CPT>, smem_bytes(a, 16, bd, CPT));
   if (err != cudaSuccess) return err;
-  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quant_scatter_kernel<GSZ, FMT>, bd,
-                                                      smem_bytes(a, 16, bd));
+  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quant_scatter_kernel<GSZ, FMT, CPT>, bd,
+                                                      smem_bytes(a, 16, bd, CPT));
   if (err != cudaSuccess) return err;
   if (per_sm < 1) per_sm = 1;
   int64_t grid = (int64_t)num_sms * per_sm;
@@ -615,8 +619,8 @@ cudaError_t launch_one(const ScatterArgs& a0, int num_sms, bool pdl, cudaStream_
   if (grid < 1) grid = 1;
   const int64_t ntok_max = (a.T + grid - 1) / grid;
   fit(ntok_max);
-  const size_t smem = smem_bytes(a, ntok_max, bd);
-  err = opt_in_smem(quant_scatter_kernel<GSZ, FMT>, smem);
+  const size_t smem = smem_bytes(a, ntok_max, bd, CPT);
+  err = opt_in_smem(quant_scatter_kernel<GSZ, FMT, CPT>, smem);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
@@ -628,21 +632,30 @@ cudaError_t launch_one(const ScatterArgs& a0, int num_sms, bool pdl, cudaStream_
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, quant_scatter_kernel<GSZ, FMT>, a);
+  return cudaLaunchKernelEx(&cfg, quant_scatter_kernel<GSZ, FMT, CPT>, a);
+}
+
+template <int CPT>
+cudaError_t launch_cpt(const ScatterArgs& a, int g, int fmt, int num_sms, bool pdl, cudaStream_t s) {
+  if (g == 128) {
+    if (fmt == kFmtPacked) return launch_one<128, kFmtPacked, CPT>(a, num_sms, pdl, s);
+    if (fmt == kFmtU8) return launch_one<128, kFmtU8, CPT>(a, num_sms, pdl, s);
+    if (fmt == kFmtF32) return launch_one<128, kFmtF32, CPT>(a, num_sms, pdl, s);
+    return launch_one<128, kFmtF32Pow2, CPT>(a, num_sms, pdl, s);
+  }
+  if (fmt == kFmtMX) return launch_one<32, kFmtMX, CPT>(a, num_sms, pdl, s);
+  return launch_one<32, kFmtU8, CPT>(a, num_sms, pdl, s);
 }
 
 }  // namespace
 
 cudaError_t launch_quant_scatter(const ScatterArgs& a, int g, int fmt, int num_sms,
                                  bool after_route_plan, cudaStream_t s) {
-  if (g == 128) {
-    if (fmt == kFmtPacked) return launch_one<128, kFmtPacked>(a, num_sms, after_route_plan, s);
-    if (fmt == kFmtU8) return launch_one<128, kFmtU8>(a, num_sms, after_route_plan, s);
-    if (fmt == kFmtF32) return launch_one<128, kFmtF32>(a, num_sms, after_route_plan, s);
-    return launch_one<128, kFmtF32Pow2>(a, num_sms, after_route_plan, s);
-  }
-  if (fmt == kFmtMX) return launch_one<32, kFmtMX>(a, num_sms, after_route_plan, s);
-  return launch_one<32, kFmtU8>(a, num_sms, after_route_plan, s);
+  // Narrow rows: one chunk per thread, so a CTA still has enough threads to
+  // keep loads in flight (measured on GB300: H = 2048 dispatch 67 -> 59 us;
+  // at H = 7168 two chunks per thread are faster, 105 against 109 us).
+  if (a.H <= MOEPERM_SCATTER_CPT1_MAX_H) return launch_cpt<1>(a, g, fmt, num_sms, after_route_plan, s);
+  return launch_cpt<2>(a, g, fmt, num_sms, after_route_plan, s);
 }
 
 }  // namespace moeperm

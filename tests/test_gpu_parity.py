@@ -900,6 +900,33 @@ def test_dispatch_max_hidden(dev, ref, T, K):                       # direct (K*
     masked_both(dev, ref, x, ids, w, H, K, 16, L, 8, 128, "u8")
 
 
+@pytest.mark.parametrize("H,g,fmt", [(5120, 128, "packed"), (5248, 128, "packed"),
+                                     (5120, 32, "mx"), (5152, 32, "u8")])
+def test_scatter_chunks_per_thread_boundary(dev, ref, H, g, fmt):
+    """Rows of at most 5120 elements run the scatter with one 16-element chunk
+    per thread (320 threads at 5120), wider ones with two (5248: 164 threads
+    rounded up to 192, the last warp partly idle). Compact (staged, K*L/E = 4),
+    masked with direct stores (K*L/E = 1) and the live-row quantiser."""
+    rng = np.random.default_rng(H + g)
+    T, K = 700, 4
+    x = synth.normal_bf16(rng, (T, H), outlier_frac=0.01)
+    ids = synth.zipf_topk(rng, T, 64, K, n_empty=4)
+    w = synth.softmax_weights(rng, T, K)
+    compact_both(dev, ref, x, ids, w, H, K, 64, 64, 128, g, fmt)
+    masked_both(dev, ref, x, ids, w, H, K, 64, 16, 256, g, fmt)
+    G = H // g
+    rxq = np.full((T, H), 0xEE, np.uint8)
+    rsc, ld = ref.scale_buffer(fmt, T, G, fill=0x5A)
+    ref.quant_group(x, T, 613, H, g, fmt, rxq, rsc, ld)
+    dxq, dsc = to_dev(rxq.copy()), to_dev(rsc.copy())
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    nl = torch.tensor([613], dtype=torch.int32, device=DEV)
+    assert dev.moe_quant_group(bf16_dev(x), H, T, nl, H, g, fmt, dxq, dsc, ld, st) == 0
+    torch.cuda.synchronize()
+    assert_same("xq", to_host(dxq, rxq), rxq)
+    assert_same("scales", to_host(dsc, rsc), rsc)
+
+
 @pytest.mark.parametrize("T", [64, 100])     # 2048 slots: one launch; 3200: two launches
 def test_dispatch_max_topk_and_experts(dev, ref, T):
     """K = 32 slots per token over L = 1024 local experts."""
