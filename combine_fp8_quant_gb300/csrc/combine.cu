@@ -10,10 +10,12 @@
 // same source rows. Lane k < K holds slot k's row and weight and broadcasts
 // them with shuffles; the slots of the warp's NEXT unit are loaded while the
 // current unit is processed, so their latency never sits in front of the row
-// loads. Each lane issues the 16-byte loads of up to 4 source rows before the
-// first FMA (4 rows in flight with 32 warps per SM measured faster than 8 rows
-// with 24 warps on the 8192-token prefill workload). y is read once per kept slot and out written once: the kernel is
-// bound by HBM reads.
+// loads. Each lane issues the 16-byte loads of a batch of source rows before
+// the batch's FMAs: at most 4 rows (4 rows in flight with 32 warps per SM
+// measured faster than 8 rows with 24 warps on the 8192-token prefill
+// workload), in ceil(K/4) batches of equal size (top-6 as 3 + 3 rather than
+// 4 + 2: 96% of the copy bandwidth instead of 93%). y is read once per kept
+// slot and out written once: the kernel is bound by HBM reads.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -22,13 +24,13 @@ namespace moeperm {
 namespace {
 
 #ifndef MOEPERM_COMBINE_BATCH
-#define MOEPERM_COMBINE_BATCH 4
+#define MOEPERM_COMBINE_BATCH 4   // largest batch of source rows in flight per lane
 #endif
+static_assert(MOEPERM_COMBINE_BATCH >= 1 && MOEPERM_COMBINE_BATCH <= 8, "batch of 1 to 8 rows");
 #ifndef MOEPERM_COMBINE_MIN_BLOCKS
 #define MOEPERM_COMBINE_MIN_BLOCKS 4
 #endif
 constexpr int kThreads = 256;
-constexpr int kBatch = MOEPERM_COMBINE_BATCH;   // source rows in flight per lane
 
 struct Slot {
   int row;
@@ -51,6 +53,7 @@ __device__ __forceinline__ Slot load_slot(const CombineArgs& p, int t, int n_liv
   return s;
 }
 
+template <int kBatch>  // source rows in flight per lane
 __global__ void __launch_bounds__(kThreads, MOEPERM_COMBINE_MIN_BLOCKS) combine_kernel(CombineArgs p) {
   const int lane = threadIdx.x & 31;
   const int gwarp = (int)((blockIdx.x * kThreads + threadIdx.x) >> 5);
@@ -113,12 +116,11 @@ __global__ void __launch_bounds__(kThreads, MOEPERM_COMBINE_MIN_BLOCKS) combine_
   }
 }
 
-}  // namespace
-
-cudaError_t launch_combine(const CombineArgs& a, int num_sms, cudaStream_t s) {
+template <int kBatch>
+cudaError_t launch_batch(const CombineArgs& a, int num_sms, cudaStream_t s) {
   int per_sm = 0;
   cudaError_t err =
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, combine_kernel, kThreads, 0);
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, combine_kernel<kBatch>, kThreads, 0);
   if (err != cudaSuccess) return err;
   if (per_sm < 1) per_sm = 1;
   const int64_t spt = (a.H / 8 + 31) / 32;
@@ -127,8 +129,23 @@ cudaError_t launch_combine(const CombineArgs& a, int num_sms, cudaStream_t s) {
   const int64_t need = (units + (kThreads / 32) - 1) / (kThreads / 32);
   if (grid > need) grid = need;
   if (grid < 1) grid = 1;
-  combine_kernel<<<(unsigned)grid, kThreads, 0, s>>>(a);
+  combine_kernel<kBatch><<<(unsigned)grid, kThreads, 0, s>>>(a);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const CombineArgs& a, int num_sms, cudaStream_t s) {
+  // the fewest batches of at most MOEPERM_COMBINE_BATCH rows, of equal size
+  const int nb = (a.K + MOEPERM_COMBINE_BATCH - 1) / MOEPERM_COMBINE_BATCH;
+  const int batch = (a.K + nb - 1) / nb;
+  switch (batch) {
+    case 1: return launch_batch<1>(a, num_sms, s);
+    case 2: return launch_batch<2 <= MOEPERM_COMBINE_BATCH ? 2 : 1>(a, num_sms, s);
+    case 3: return launch_batch<3 <= MOEPERM_COMBINE_BATCH ? 3 : 1>(a, num_sms, s);
+    case 4: return launch_batch<4 <= MOEPERM_COMBINE_BATCH ? 4 : 1>(a, num_sms, s);
+    default: return launch_batch<MOEPERM_COMBINE_BATCH>(a, num_sms, s);
+  }
 }
 
 }  // namespace moeperm

@@ -349,7 +349,9 @@ def test_dispatch_masked_live_tokens(dev, ref):
 # combine
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("K", [1, 3, 8, 13])
+# K selects the row batch of the combine: ceil(K / ceil(K/4)) rows in flight,
+# so 1..4 run one batch, 5..8 two equal ones (3+3, 4+4, 3+2, 4+3), 9..12 three
+@pytest.mark.parametrize("K", [1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 13, 32])
 def test_combine_random_rows(dev, ref, K):
     rng = np.random.default_rng(K)
     T, H, R = 77, 1536, 500
