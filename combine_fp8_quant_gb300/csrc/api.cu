@@ -59,7 +59,7 @@ moe_status_t check_common(const DispatchCommon& c) {
   if (!fmt_ok(c.fmt, c.g)) return MOE_ERR_INVALID_ARG;
   if (c.K < 1 || c.K > kMaxK || c.L < 1 || c.L > kMaxL || c.E < c.L) return MOE_ERR_INVALID_ARG;
   if ((int64_t)c.T * c.K > kMaxAssignments || c.H > kMaxHidden) return MOE_ERR_INVALID_ARG;
-  if (route_geometry((int64_t)c.T * c.K, c.L, route_table_pref(c.H)).S == 0) return MOE_ERR_INVALID_ARG;
+  if (route_geometry((int64_t)c.T * c.K, c.L, route_table_pref(c.H, c.L)).S == 0) return MOE_ERR_INVALID_ARG;
   if (c.T > 0) {
     if (!c.x || !aligned16(c.x) || c.ldx < c.H || c.ldx % 8) return MOE_ERR_INVALID_ARG;
     if (!c.ids || !c.src2dst) return MOE_ERR_INVALID_ARG;
@@ -89,7 +89,7 @@ moe_status_t run_dispatch(const DispatchCommon& c, int mode, int32_t block_e, in
     sa.masked_m = masked_m; sa.status = d_status;
     return cuda_status(launch_dispatch_small(sa, c.g, c.fmt, sms, stream));
   }
-  const RouteGeom geom = route_geometry(A, c.L, route_table_pref(c.H));
+  const RouteGeom geom = route_geometry(A, c.L, route_table_pref(c.H, c.L));
   int32_t* table = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(c.ws) + kWsHeader);
 
   RoutePlanArgs rp{};
@@ -135,11 +135,11 @@ size_t moe_scale_bytes(moe_scale_fmt_t fmt, int64_t rows, int32_t H, int32_t g) 
 size_t moe_workspace_bytes(int32_t T, int32_t K, int32_t L) {
   if (T < 0 || K < 1 || L < 1) return 0;
   const int64_t A = (int64_t)T * K;
-  // the larger table of the two row-width preferences, so one workspace fits
-  // every H (a preference that no chain meets falls back to the shortest
-  // chain under the hard limit, which can be the larger table)
+  // the larger table of the two preferences, so one workspace fits every H
+  // (a preference that no chain meets falls back to the shortest chain under
+  // the hard limit, which can be the larger table)
   int64_t nc = 0;
-  for (int64_t pref : {route_table_pref(kNarrowRow - 16), route_table_pref(kNarrowRow)}) {
+  for (int64_t pref : {(int64_t)MOEPERM_ROUTE_TABLE_PREF_SMALL, (int64_t)MOEPERM_ROUTE_TABLE_PREF}) {
     const RouteGeom geom = route_geometry(A, L, pref);
     if (geom.S == 0) return 0;
     if (geom.nchunks > nc) nc = geom.nchunks;

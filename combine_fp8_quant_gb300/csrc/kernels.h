@@ -35,18 +35,22 @@ struct RouteGeom {
 };
 // The shortest chain S whose table (chunks x L) fits table_pref ints, else
 // the shortest whose table fits kMaxTableInts. A smaller table costs a longer
-// chain but less shared memory and fewer table loads in every scatter CTA;
-// narrow rows (many small scatter CTAs per SM, each loading the table) prefer
-// the smaller one. Measured on GB300 across T, H, E, top-k shapes.
+// chain but less shared memory and fewer table loads in every scatter CTA.
+// Measured on GB300 across T, H, L, E and top-k: a token with few kept slots
+// (L <= 128 local experts) or a narrow row gives each scatter CTA little work
+// per token, so its loop is latency-bound and the residency that a small
+// table leaves (4 rather than 3 CTAs per SM at H = 7168) decides; with more
+// experts the loop is bandwidth-bound and the shorter chain wins.
 #ifndef MOEPERM_ROUTE_TABLE_PREF
 #define MOEPERM_ROUTE_TABLE_PREF 8192
 #endif
-#ifndef MOEPERM_ROUTE_TABLE_PREF_NARROW
-#define MOEPERM_ROUTE_TABLE_PREF_NARROW 2048
+#ifndef MOEPERM_ROUTE_TABLE_PREF_SMALL
+#define MOEPERM_ROUTE_TABLE_PREF_SMALL 2048
 #endif
-constexpr int kNarrowRow = 4096;   // H below this: the narrow-row preference
-inline int64_t route_table_pref(int H) {
-  return H < kNarrowRow ? MOEPERM_ROUTE_TABLE_PREF_NARROW : MOEPERM_ROUTE_TABLE_PREF;
+constexpr int kNarrowRow = 4096;   // H below this: the small-table preference
+constexpr int kFewExperts = 128;   // L up to this: the small-table preference
+inline int64_t route_table_pref(int H, int L) {
+  return (H < kNarrowRow || L <= kFewExperts) ? MOEPERM_ROUTE_TABLE_PREF_SMALL : MOEPERM_ROUTE_TABLE_PREF;
 }
 RouteGeom route_geometry(int64_t A, int L, int64_t table_pref);
 cudaError_t launch_route_plan(const RoutePlanArgs& a, const RouteGeom& g, cudaStream_t s);
