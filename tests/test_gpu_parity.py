@@ -874,6 +874,20 @@ def test_dispatch_max_assignments(dev, ref):
     compact_both(dev, ref, x, ids, w, H, K, L + 2, L, 128, 128, "packed", with_rw=False)
 
 
+# Each case selects one route-plan chain length (slots per lane S) at 32 warps
+# per CTA, with the small-table preference of narrow rows (<= 2048 entries):
+# 3000 slots x 16 experts: S = 1 (3 chunks); then 64 experts at 40000 / 100000 /
+# 200000 / 400000 slots: S = 2 / 4 / 8 / 16 (20 to 25 chunks).
+@pytest.mark.parametrize("T,L", [(375, 16), (5000, 64), (12500, 64), (25000, 64), (50000, 64)])
+def test_dispatch_route_chain_lengths(dev, ref, T, L):
+    rng = np.random.default_rng(T + L)
+    K, H = 8, 128
+    x = synth.normal_bf16(rng, (T, H))
+    ids = synth.zipf_topk(rng, T, L, K, n_empty=2)
+    w = synth.softmax_weights(rng, T, K)
+    compact_both(dev, ref, x, ids, w, H, K, L, L, 128, 128, "packed")
+
+
 def test_dispatch_long_route_chain(dev, ref):
     """1024 local experts x 262144 slots: only 8 warps fit the per-warp
     histograms, so each lane walks 64 slots (16 chunks of 16384, a full
