@@ -4,9 +4,92 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "../../include/moeperm.h"
 #include "common.cuh"
 #include "kernels.h"
+
+// Host-side caches of launch queries, per device. An occupancy query or a
+// device attribute read costs the host about as much as a launch, and a
+// shared-memory opt-in more; each is asked once per key. The tables are
+// small and fixed: once one is full, new keys are simply asked every time.
+namespace moeperm {
+namespace {
+std::mutex g_cache_mu;
+struct OccEntry { const void* kernel; int threads; size_t smem; int dev; int value; };
+OccEntry g_occ[256];
+int g_nocc = 0;
+struct SmemEntry { const void* kernel; int dev; size_t dyn; };
+SmemEntry g_smem[128];
+int g_nsmem = 0;
+struct AttrEntry { int attr; int dev; int value; };
+AttrEntry g_attr[64];
+int g_nattr = 0;
+}  // namespace
+
+cudaError_t occupancy_cached(const void* kernel, int threads, size_t smem, int* per_sm) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  {
+    std::lock_guard<std::mutex> g(g_cache_mu);
+    for (int i = 0; i < g_nocc; ++i) {
+      const OccEntry& e = g_occ[i];
+      if (e.kernel == kernel && e.threads == threads && e.smem == smem && e.dev == dev) {
+        *per_sm = e.value;
+        return cudaSuccess;
+      }
+    }
+  }
+  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, kernel, threads, smem);
+  if (err != cudaSuccess) return err;
+  std::lock_guard<std::mutex> g(g_cache_mu);
+  if (g_nocc < 256) g_occ[g_nocc++] = OccEntry{kernel, threads, smem, dev, *per_sm};
+  return cudaSuccess;
+}
+
+cudaError_t opt_in_smem_cached(const void* kernel, size_t dyn) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  {
+    std::lock_guard<std::mutex> g(g_cache_mu);
+    for (int i = 0; i < g_nsmem; ++i)
+      if (g_smem[i].kernel == kernel && g_smem[i].dev == dev && g_smem[i].dyn >= dyn) return cudaSuccess;
+  }
+  err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+  if (err != cudaSuccess) return err;
+  std::lock_guard<std::mutex> g(g_cache_mu);
+  for (int i = 0; i < g_nsmem; ++i)
+    if (g_smem[i].kernel == kernel && g_smem[i].dev == dev) {
+      if (g_smem[i].dyn < dyn) g_smem[i].dyn = dyn;
+      return cudaSuccess;
+    }
+  if (g_nsmem < 128) g_smem[g_nsmem++] = SmemEntry{kernel, dev, dyn};
+  return cudaSuccess;
+}
+
+cudaError_t device_attr_cached(cudaDeviceAttr attr, int* value) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  {
+    std::lock_guard<std::mutex> g(g_cache_mu);
+    for (int i = 0; i < g_nattr; ++i)
+      if (g_attr[i].attr == (int)attr && g_attr[i].dev == dev) {
+        *value = g_attr[i].value;
+        return cudaSuccess;
+      }
+  }
+  err = cudaDeviceGetAttribute(value, attr, dev);
+  if (err != cudaSuccess) return err;
+  std::lock_guard<std::mutex> g(g_cache_mu);
+  if (g_nattr < 64) g_attr[g_nattr++] = AttrEntry{(int)attr, dev, *value};
+  return cudaSuccess;
+}
+
+}  // namespace moeperm
 
 using namespace moeperm;
 
@@ -21,15 +104,8 @@ constexpr size_t kWsHeader = 256;  // reserved header before the chunk table
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int num_sms_cached() {
-  static int cache[128] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 0;
-  if (cache[dev] == 0) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    cache[dev] = n;
-  }
-  return cache[dev];
+  int n = 0;
+  return device_attr_cached(cudaDevAttrMultiProcessorCount, &n) == cudaSuccess ? n : 0;
 }
 
 bool fmt_ok(int fmt, int g) {

@@ -119,8 +119,7 @@ __global__ void __launch_bounds__(kThreads, MOEPERM_COMBINE_MIN_BLOCKS) combine_
 template <int kBatch>
 cudaError_t launch_batch(const CombineArgs& a, int num_sms, cudaStream_t s) {
   int per_sm = 0;
-  cudaError_t err =
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, combine_kernel<kBatch>, kThreads, 0);
+  cudaError_t err = occupancy(combine_kernel<kBatch>, kThreads, 0, &per_sm);
   if (err != cudaSuccess) return err;
   if (per_sm < 1) per_sm = 1;
   const int64_t spt = (a.H / 8 + 31) / 32;

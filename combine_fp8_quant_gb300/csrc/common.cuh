@@ -227,13 +227,22 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// Lets a kernel take `dyn` bytes of dynamic shared memory. Without the
-// opt-in a CTA is limited to 48 KiB of dynamic plus static shared memory; the
-// static arrays of these kernels stay under 1 KiB.
+// Host-side launch queries, cached per device (they cost more host time than
+// a launch; api.cu): resident CTAs per SM for (kernel, threads, dynamic shared
+// memory), and the opt-in that lets a kernel take `dyn` bytes of dynamic shared
+// memory. Without the opt-in a CTA is limited to 48 KiB of dynamic plus static
+// shared memory; the static arrays of these kernels stay under 1 KiB.
+cudaError_t occupancy_cached(const void* kernel, int threads, size_t smem, int* per_sm);
+cudaError_t opt_in_smem_cached(const void* kernel, size_t dyn);
+cudaError_t device_attr_cached(cudaDeviceAttr attr, int* value);
 template <typename Kern>
 inline cudaError_t opt_in_smem(Kern kernel, size_t dyn) {
   if (dyn + 1024 <= 48 * 1024) return cudaSuccess;
-  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+  return opt_in_smem_cached(reinterpret_cast<const void*>(kernel), dyn);
+}
+template <typename Kern>
+inline cudaError_t occupancy(Kern kernel, int threads, size_t smem, int* per_sm) {
+  return occupancy_cached(reinterpret_cast<const void*>(kernel), threads, smem, per_sm);
 }
 
 __device__ __forceinline__ int64_t align_up64(int64_t c, int64_t b) { return (c + b - 1) / b * b; }

@@ -255,8 +255,7 @@ cudaError_t launch_s(const ScatterArgs& a, int num_sms, cudaStream_t s) {
   cudaError_t err = opt_in_smem(dispatch_small_kernel<GSZ, FMT, S>, smem);
   if (err != cudaSuccess) return err;
   int per_sm = 0;
-  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      &per_sm, dispatch_small_kernel<GSZ, FMT, S>, kThreads, smem);
+  err = occupancy(dispatch_small_kernel<GSZ, FMT, S>, kThreads, smem, &per_sm);
   if (err != cudaSuccess) return err;
   if (per_sm < 1) per_sm = 1;
   int64_t grid = (int64_t)num_sms * per_sm;

@@ -583,9 +583,8 @@ cudaError_t launch_one(const ScatterArgs& a0, int num_sms, bool pdl, cudaStream_
   int bd = (nch + CPT - 1) / CPT;
   bd = (bd + 31) / 32 * 32;
   if (bd > 1024) return cudaErrorInvalidValue;  // H > 32768 is rejected on the host
-  int dev = 0, optin = 0;
-  cudaError_t err = cudaGetDevice(&dev);
-  if (err == cudaSuccess) err = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  int optin = 0;
+  cudaError_t err = device_attr_cached(cudaDevAttrMaxSharedMemoryPerBlockOptin, &optin);
   if (err != cudaSuccess) return err;
   const size_t budget = (size_t)optin - 1024;  // room for the static arrays
   // Resident CTAs per SM with a provisional row buffer of 16 tokens per CTA;
@@ -610,8 +609,7 @@ cudaError_t launch_one(const ScatterArgs& a0, int num_sms, bool pdl, cudaStream_
   int per_sm = 0;
   err = opt_in_smem(quant_scatter_kernel<GSZ, FMT, CPT>, smem_bytes(a, 16, bd, CPT));
   if (err != cudaSuccess) return err;
-  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quant_scatter_kernel<GSZ, FMT, CPT>, bd,
-                                                      smem_bytes(a, 16, bd, CPT));
+  err = occupancy(quant_scatter_kernel<GSZ, FMT, CPT>, bd, smem_bytes(a, 16, bd, CPT), &per_sm);
   if (err != cudaSuccess) return err;
   if (per_sm < 1) per_sm = 1;
   int64_t grid = (int64_t)num_sms * per_sm;

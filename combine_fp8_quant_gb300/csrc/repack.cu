@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(kThreads, MOEPERM_REPACK_MIN_BLOCKS) repack_ke
 cudaError_t launch_repack(const RepackArgs& a, int num_sms, cudaStream_t s) {
   const size_t smem = (size_t)2 * a.L * sizeof(int32_t);
   int per_sm = 0;
-  cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, repack_kernel, kThreads, smem);
+  cudaError_t err = occupancy(repack_kernel, kThreads, smem, &per_sm);
   if (err != cudaSuccess) return err;
   if (per_sm < 1) per_sm = 1;
   int64_t grid = (int64_t)num_sms * per_sm;

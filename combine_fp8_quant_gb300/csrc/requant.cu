@@ -179,7 +179,7 @@ __global__ void __launch_bounds__(kThreads, MOEPERM_REQUANT_MIN_BLOCKS) requant_
 template <typename Kern>
 cudaError_t launch_rows(Kern k, const RequantArgs& a, int num_sms, cudaStream_t s) {
   int per_sm = 0;
-  cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kThreads, 0);
+  cudaError_t err = occupancy(k, kThreads, 0, &per_sm);
   if (err != cudaSuccess) return err;
   if (per_sm < 1) per_sm = 1;
   int64_t grid = (int64_t)num_sms * per_sm;

@@ -94,20 +94,31 @@ def lib():
 
 def _ptr(t):
     """Device address of a CUDA tensor (or a raw integer address, or None).
-    A CPU tensor is rejected here: its host address would reach a kernel."""
+    A CPU tensor is rejected here: its host address would reach a kernel.
+    Plain integers go to ctypes as they are (a void* argument accepts them)."""
     if t is None:
         return None
-    if isinstance(t, int):
-        return C.c_void_p(t)
-    if t.device.type != "cuda":
+    if type(t) is int:
+        return t
+    if not t.is_cuda:
         raise ValueError(f"moeperm: tensor on {t.device}, but every tensor argument must be on "
                          "a CUDA device")
-    return C.c_void_p(t.data_ptr())
+    return t.data_ptr()
+
+
+# The current stream's raw handle without building a torch Stream object (the
+# public call costs microseconds per launch on small problems); the public
+# call is the fallback where these functions are absent.
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+_cur_device = getattr(torch._C, "_cuda_getDevice", None)
 
 
 def _stream(stream=None):
-    s = torch.cuda.current_stream() if stream is None else stream
-    return C.c_void_p(s.cuda_stream)
+    if stream is not None:
+        return stream.cuda_stream
+    if _raw_stream is not None and _cur_device is not None:
+        return _raw_stream(_cur_device())
+    return torch.cuda.current_stream().cuda_stream
 
 
 def _check(code: int, where: str):
