@@ -253,11 +253,13 @@ def scale_tensor(fmt: str, rows: int, H: int, g: int, device, blocks: int = 1, l
 
 
 class Workspace:
-    """Zero-initialised dispatch workspace, reusable across calls on one stream."""
+    """Dispatch workspace, reusable across calls on one stream. Every dispatch
+    writes the chunk table before reading it, so no initialisation is needed
+    (no fill kernel per allocation)."""
 
     def __init__(self, T: int, K: int, L: int, device):
         self.nbytes = moe_workspace_bytes(T, K, L)
-        self.buf = torch.zeros(self.nbytes, dtype=torch.uint8, device=device)
+        self.buf = torch.empty(self.nbytes, dtype=torch.uint8, device=device)
 
     def fits(self, T, K, L):
         return moe_workspace_bytes(T, K, L) <= self.nbytes
