@@ -791,16 +791,14 @@ def test_graph_capture_scatter_above_48k_shared_memory(dev, ref):
 # Full size, in the benchmark's launch configuration (prefill workload)
 # ---------------------------------------------------------------------------
 
-def test_prefill_full_size_sampled(dev, ref):
-    """T = 8192, H = 7168, 256 local experts, top-8 Zipf routing, block_e 128,
-    packed UE8M0 -- the call bench.py times. The layout does not depend on H,
-    so the oracle run on the first 128 columns gives the full layout and the
-    first group of every row bit-exactly; sampled tokens are checked over the
-    whole row (payload, all 56 scales) and through the combine."""
-    d = synth.prefill(0)
-    c = d["cfg"]
-    T, H, K, E, L, b, g = c["T"], c["H"], c["K"], c["E"], c["L"], c["block_e"], c["g"]
-    x, ids, w = d["x"], d["topk_ids"], d["topk_weights"]
+def full_size_sampled(dev, ref, x, ids, w, E, L, b=128, g=128):
+    """Compact dispatch + combine at full size, checked without running the
+    oracle over every byte. The layout does not depend on H, so the oracle run
+    on the first 128 columns gives the full layout and the first group of
+    every row bit-exactly; sampled tokens are checked over the whole row
+    (payload, every scale) and through the combine."""
+    T, H = x.shape
+    K = ids.shape[1]
     out = dev.dispatch_compact(bf16_dev(x), to_dev(ids), to_dev(w), E, L, block_e=b, group_size=g,
                                scale_fmt="packed")
     torch.cuda.synchronize()
@@ -856,6 +854,29 @@ def test_prefill_full_size_sampled(dev, ref):
                                np.ascontiguousarray(w[t:t + 1]), 1, K, H)
         got = o[t].view(torch.int16).cpu().numpy().view(np.uint16)
         assert np.array_equal(got, want[0])
+
+
+
+
+def test_prefill_full_size_sampled(dev, ref):
+    """T = 8192, H = 7168, 256 local experts, top-8 Zipf routing, block_e 128,
+    packed UE8M0: the call bench.py times."""
+    d = synth.prefill(0)
+    c = d["cfg"]
+    assert (c["block_e"], c["g"]) == (128, 128)
+    full_size_sampled(dev, ref, d["x"], d["topk_ids"], d["topk_weights"], c["E"], c["L"])
+
+
+@pytest.mark.parametrize("T,H,E,K", [(16384, 2048, 64, 6), (8192, 5120, 160, 6)])
+def test_sweep_shapes_full_size_sampled(dev, ref, T, H, E, K):
+    """Two shapes of the shape sweep at full size: narrow rows (one chunk per
+    scatter thread, the small route-plan table) and top-6 over 160 experts
+    (3 + 3 row batches in the combine)."""
+    rng = np.random.default_rng(T + H + E + K)
+    x = synth.normal_bf16(rng, (T, H))
+    ids = synth.zipf_topk(rng, T, E, K, n_empty=12)
+    w = synth.softmax_weights(rng, T, K)
+    full_size_sampled(dev, ref, x, ids, w, E, E)
 
 
 # ---------------------------------------------------------------------------
