@@ -83,3 +83,44 @@ def test_random_repack(dev, ref, seed):
         exp = rng.integers(0, 256, size=(R, H), dtype=np.uint8)
         exp[(exp & 0x7F) == 0x7F] = 0x22
         repack_both(dev, ref, exp, 1, H, psum, L, align, cap)
+
+
+def draw_wide(rng):
+    """Rows up to 8192 elements (the scatter's one- and two-chunk-per-thread
+    paths), up to 300 local experts (both route-plan table preferences),
+    up to 3000 tokens, uniform or Zipf routing."""
+    g = int(rng.choice([128, 32]))
+    H = g * int(rng.integers(1, 8192 // g + 1))
+    T = int(rng.choice([int(rng.integers(1, 64)), int(rng.integers(300, 3000))]))
+    K = int(rng.integers(1, 10))
+    L = int(rng.integers(1, 300))
+    E = L + int(rng.integers(0, 60))
+    return g, H, T, K, L, E, str(rng.choice(FMTS[g]))
+
+
+# Seeds picked (by drawing on the CPU) so that each covers a path: narrow rows
+# on two launches (71002), one launch with wide rows (71004), one chunk per
+# thread with > 128 experts (71006), group 32 on two launches (71011), two
+# chunks per thread with <= 128 / > 128 experts (71012 / 71058), fp32 scales
+# and packed UE8M0 on two launches with > 128 experts (71039 / 71078).
+@pytest.mark.parametrize("seed", [71002, 71004, 71006, 71011, 71012, 71039, 71058, 71078])
+def test_random_wide_configs(dev, ref, seed):
+    rng = np.random.default_rng(seed)
+    g, H, T, K, L, E, fmt = draw_wide(rng)
+    b = int(rng.choice([1, 16, 128]))
+    ids = random_routing(rng, T, E, K)
+    if K <= E and rng.random() < 0.5:
+        ids = synth.zipf_topk(rng, T, E, K, n_empty=min(4, E - K))
+    w = synth.softmax_weights(rng, T, K)
+    x = synth.normal_bf16(rng, (T, H), outlier_frac=0.01)
+    bound = ref.compact_bound(T * K, L, b)
+    if bound * H > 400_000_000:      # keeps the oracle's whole-buffer copy small
+        pytest.skip("buffer above the test's size limit")
+    r, _, _ = compact_both(dev, ref, x, ids, w, H, K, E, L, b, g, fmt)
+    y = synth.normal_bf16(rng, (max(bound, 1), H))
+    check_combine(dev, ref, y, r["s2d"], w, H)
+    kept = ids[(ids >= 0) & (ids < L)]
+    top = int(np.bincount(kept, minlength=L).max()) if kept.size else 0
+    cap = max(1, top if rng.random() < 0.7 else top // 2)
+    if L * cap * H <= 200_000_000:
+        masked_both(dev, ref, x, ids, w, H, K, E, L, cap, g, fmt)
