@@ -136,3 +136,30 @@ def test_size_limits_rejected(mp):
     # chunk table beyond 64 KiB: 1024 experts with 2^19 slots
     assert mp.moe_workspace_bytes(65536, 8, 1024) == 0
     assert call_compact(mp, T=65536, L=1024, E=1024, workspace_bytes=1 << 24) == mp.MOE_ERR_INVALID_ARG
+
+
+def _route_geometry_table(A, L, pref):
+    """The route-plan geometry rule restated: the shortest chain S (slots per
+    lane) in 1, 2, 4, 8, 16 at up to 32 warps (fewer when warps x L would pass
+    12288 histogram entries), or 64 at up to 8 warps, whose table (chunks x L)
+    fits `pref` entries, else the shortest whose table fits 16384."""
+    wmax = 1 if L >= 12288 else min(32, 12288 // L)
+    for limit in (pref, 16384):
+        for S in (1, 2, 4, 8, 16, 64):
+            W = min(wmax, 8 if S > 16 else 32)
+            chunk = 32 * W * S
+            nc = max(1, -(-A // chunk))
+            if nc * L <= limit:
+                return nc * L
+    return None
+
+
+@pytest.mark.parametrize("T,K,L", [(300, 8, 256), (8192, 8, 256), (8192, 8, 128), (8192, 8, 32),
+                                   (16384, 6, 64), (32768, 8, 256), (131072, 8, 256), (8192, 32, 1024),
+                                   (1000, 3, 1), (4096, 8, 160), (50000, 8, 64), (9999, 7, 333)])
+def test_workspace_bytes_follow_the_route_geometry(mp, T, K, L):
+    """One workspace serves every row width: it holds the larger chunk table of
+    the two table preferences (2048 entries for narrow rows or <= 128 local
+    experts, 8192 otherwise)."""
+    want = max(_route_geometry_table(T * K, L, 2048), _route_geometry_table(T * K, L, 8192))
+    assert mp.moe_workspace_bytes(T, K, L) == 256 + 4 * want
