@@ -173,13 +173,14 @@ moe_status_t run_dispatch(const DispatchCommon& c, int mode, int32_t block_e, in
   rp.T = c.T; rp.K = c.K; rp.L = c.L;
   rp.chunk = geom.chunk; rp.nchunks = (int32_t)geom.nchunks;
   rp.lrank = c.src2dst; rp.table = table; rp.status = d_status;
+  rp.queue = reinterpret_cast<int32_t*>(c.ws);  // first word of the reserved header
   if (launch_route_plan(rp, geom, stream) != cudaSuccess) return MOE_ERR_CUDA;
 
   ScatterArgs sa{};
   sa.x = static_cast<const uint16_t*>(c.x); sa.ldx = c.ldx; sa.T = c.T;
   sa.d_num_tokens = c.d_num_tokens; sa.H = c.H; sa.ids = c.ids; sa.w = c.w;
   sa.K = c.K; sa.L = c.L; sa.E = c.E; sa.mode = mode; sa.block_e = block_e; sa.cap = cap;
-  sa.chunk = rp.chunk; sa.nchunks = rp.nchunks; sa.table = table;
+  sa.chunk = rp.chunk; sa.nchunks = rp.nchunks; sa.table = table; sa.queue = rp.queue;
   sa.xq = static_cast<uint8_t*>(c.xq); sa.scales = c.scales; sa.ld_s = c.ld_s;
   sa.src2dst = c.src2dst; sa.row_weights = c.row_weights;
   sa.m_indices = m_indices; sa.bound = bound;

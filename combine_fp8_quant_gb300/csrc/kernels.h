@@ -24,6 +24,7 @@ struct RoutePlanArgs {
   int32_t* lrank;              // [T*K] out: stable rank inside the chunk, -1 dropped
   int32_t* table;              // [nchunks, L] out: chunk histogram
   int32_t* status;
+  int32_t* queue;              // optional: set to 0 (the scatter's token counter)
 };
 // Launch geometry of the route plan: S slots per lane (the length of each
 // warp's dependent chain), warps per CTA, chunk = 32 * warps * S slots per CTA.
@@ -87,6 +88,8 @@ struct ScatterArgs {
   int32_t* status;
   int32_t stages, pre;         // scatter: staging ring size, tokens staged before the wait
   int32_t direct;              // scatter: 1 = direct stores, no staging (few kept slots per token)
+  int32_t* queue;              // direct mode: token counter, reset to 0 by the route plan
+  int32_t dyn;                 // direct mode: tokens taken from the counter (set at launch)
 };
 cudaError_t launch_quant_scatter(const ScatterArgs& a, int g, int fmt, int num_sms,
                                  bool after_route_plan, cudaStream_t s);

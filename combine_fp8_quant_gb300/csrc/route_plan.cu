@@ -50,6 +50,7 @@ __global__ void __launch_bounds__(32 * max_warps_for(S)) route_plan_kernel(Route
   const int L = p.L;
 
   for (int i = tid; i < nw * L; i += bd) smem[i] = 0;
+  if (p.queue != nullptr && blockIdx.x == 0 && tid == 0) *p.queue = 0;  // read only after this grid ends
   const int n_live = live_count(p.d_num_tokens, p.T, p.status, blockIdx.x == 0 && tid == 0);
   const int64_t A = (int64_t)p.T * p.K;
   const int64_t A_live = (int64_t)n_live * p.K;
