@@ -20,7 +20,9 @@
 //   destination per row it runs barrier-free with direct 16-byte stores, and
 //   so does a dispatch whose tokens keep few slots (K * L / E <= 3, decided on
 //   the host from scalars alone): there the per-token barrier of the staged
-//   path costs more than the bulk copies save.
+//   path costs more than the bulk copies save. For rows of two chunks per
+//   thread that direct mode takes its tokens from a counter instead of a
+//   fixed strided set, so that CTAs end together (see the loop below).
 //
 // Design: a persistent grid (SMs x resident CTAs, independent of the routing)
 // walks the live tokens, t = blockIdx.x + i * gridDim.x. One thread owns two
