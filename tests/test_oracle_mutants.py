@@ -53,6 +53,12 @@ MUTANTS = [
      "int64_t src = start[e] + j, dst = (int64_t)e * cap + (cap - 1 - j);", ["test_repack_roundtrip"]),
     ("masked_m_unclamped", "masked_m[e] = counts[e] < cap ? counts[e] : cap;", "masked_m[e] = counts[e];",
      ["test_dispatch_masked_overflow"]),
+    ("rank_order_reversed", "for (int64_t a = 0; a < (int64_t)T * K; ++a) {\n    int32_t t = (int32_t)(a / K);",
+     "for (int64_t a = (int64_t)T * K - 1; a >= 0; --a) {\n    int32_t t = (int32_t)(a / K);",
+     ["test_dispatch_compact_invariants_random", "test_dispatch_compact_exhaustive_tiny"]),
+    ("m_indices_tail_filled", "for (int64_t r = 0; r < bound; ++r) m_indices[r] = -1;",
+     "for (int64_t r = 0; r < bound; ++r) m_indices[r] = L - 1;",
+     ["test_dispatch_compact_invariants_random", "test_dispatch_compact_exhaustive_tiny"]),
     # widened rows: OCP-MX exponent, plain fp32 scales, e8m0 / amax requant, weighted repack
     ("mx_emax_off_by_one", "  int X = k - 8;", "  int X = k - 7;",
      ["test_mx_exponent_closed_forms_and_interval", "test_quant_row_mx_against_library"]),
