@@ -59,6 +59,8 @@ MUTANTS = [
     ("m_indices_tail_filled", "for (int64_t r = 0; r < bound; ++r) m_indices[r] = -1;",
      "for (int64_t r = 0; r < bound; ++r) m_indices[r] = L - 1;",
      ["test_dispatch_compact_invariants_random", "test_dispatch_compact_exhaustive_tiny"]),
+    ("overflow_flag_off_by_one", "if (counts[e] > cap) st |= REF_ST_OVERFLOW;",
+     "if (counts[e] > cap + 1) st |= REF_ST_OVERFLOW;", ["test_dispatch_masked_overflow"]),
     # widened rows: OCP-MX exponent, plain fp32 scales, e8m0 / amax requant, weighted repack
     ("mx_emax_off_by_one", "  int X = k - 8;", "  int X = k - 7;",
      ["test_mx_exponent_closed_forms_and_interval", "test_quant_row_mx_against_library"]),

@@ -393,6 +393,10 @@ def test_dispatch_masked_overflow(ref):
     # exactly at capacity: no overflow
     r = run_masked(ref, x[:8], ids[:8], w[:8], H, K, L, 8, 128, "u8")
     assert r["st"] == 0 and r["mm"].tolist() == [8, 0, 0, 0]
+    # one slot past capacity: an overflow, and that one slot is dropped
+    r = run_masked(ref, x[:7], ids[:7], w[:7], H, K, L, 6, 128, "u8")
+    assert r["st"] & ref.ST_OVERFLOW and r["mm"].tolist() == [6, 0, 0, 0]
+    assert r["s2d"][:, 0].tolist() == [0, 1, 2, 3, 4, 5, -1]
 
 
 def test_masked_and_compact_combine_identical(ref):
