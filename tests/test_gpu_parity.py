@@ -899,6 +899,22 @@ def test_dispatch_max_assignments(dev, ref):
 # per CTA, with the small-table preference of narrow rows (<= 2048 entries):
 # 3000 slots x 16 experts: S = 1 (3 chunks); then 64 experts at 40000 / 100000 /
 # 200000 / 400000 slots: S = 2 / 4 / 8 / 16 (20 to 25 chunks).
+@pytest.mark.parametrize("n_live", [None, 1777, 100, 0])
+def test_dispatch_direct_token_counter(dev, ref, n_live):
+    """Few kept slots per token (32 of 256 experts local, top-8) with rows of
+    two chunks per scatter thread: the scatter takes its tokens from the
+    counter that the route plan resets, with a device live count below the
+    token count (and below the grid: 100, and 0), compact and masked."""
+    rng = np.random.default_rng(31 + (n_live or 0))
+    T, K, E, L, H = 3000, 8, 256, 32, 7168
+    x = synth.normal_bf16(rng, (T, H), outlier_frac=0.01)
+    ids = synth.uniform_topk(rng, T, E, K)
+    w = synth.softmax_weights(rng, T, K)
+    compact_both(dev, ref, x, ids, w, H, K, E, L, 128, 128, "packed", n_live=n_live)
+    masked_both(dev, ref, x, ids, w, H, K, E, L, 128, 128, "packed", n_live=n_live)
+    compact_both(dev, ref, x, ids, w, H, K, E, L, 128, 32, "mx", n_live=n_live)
+
+
 @pytest.mark.parametrize("T,L", [(375, 16), (5000, 64), (12500, 64), (25000, 64), (50000, 64)])
 def test_dispatch_route_chain_lengths(dev, ref, T, L):
     rng = np.random.default_rng(T + L)
