@@ -92,7 +92,7 @@ def _declare(L):
         "ref_dispatch_compact": (i32, [vp, i64, i32, i32, i32, vp, vp, i32, i32, i32, i32, i32,
                                        vp, vp, i64, vp, i64, vp, vp, vp, vp, vp, vp]),
         "ref_dispatch_masked": (i32, [vp, i64, i32, i32, i32, vp, vp, i32, i32, i32, i32, i32,
-                                      vp, vp, i64, vp, vp, vp]),
+                                      vp, vp, i64, vp, vp, vp, vp, i32]),
         "ref_combine_f64": (None, [vp, i64, vp, vp, i32, i32, i32, vp, vp]),
         "ref_combine_f32": (None, [vp, i64, vp, vp, i32, i32, i32, vp]),
         "ref_requant": (None, [vp, i64, vp, i32, i32, vp, vp]),
@@ -224,11 +224,11 @@ def dispatch_compact(x, T, n_live, H, ids, w, K, L, block_e, g, fmt, xq, scales,
 
 
 def dispatch_masked(x, T, n_live, H, ids, w, K, L, cap, g, fmt, xq, scales, ld_s,
-                    masked_m, src2dst, row_weights=None, ldx=None):
+                    masked_m, src2dst, row_weights=None, ldx=None, psum=None, psum_align=128):
     ldx = H if ldx is None else ldx
     return int(lib().ref_dispatch_masked(
         _p(x), ldx, T, n_live, H, _p(ids), _p(w), K, L, cap, g, FMT[fmt], _p(xq),
-        _p(scales), ld_s, _p(masked_m), _p(src2dst), _p(row_weights)))
+        _p(scales), ld_s, _p(masked_m), _p(src2dst), _p(row_weights), _p(psum), psum_align))
 
 
 def combine_f64(y, src2dst, w, T, K, H, ldy=None):

@@ -344,7 +344,8 @@ int32_t ref_dispatch_masked(const uint16_t* x, int64_t ldx, int32_t T, int32_t n
                             int32_t H, const int32_t* topk_ids, const float* topk_weights,
                             int32_t K, int32_t L, int32_t cap, int32_t g, int32_t fmt,
                             uint8_t* xq, void* scales, int64_t ld_s, int32_t* masked_m,
-                            int32_t* src2dst, float* row_weights) {
+                            int32_t* src2dst, float* row_weights, int32_t* psum,
+                            int32_t psum_align) {
   int32_t st = 0;
   if (n_live > T) { st |= REF_ST_LIVE_OVERFLOW; n_live = T; }
   if (n_live < 0) n_live = 0;
@@ -358,6 +359,17 @@ int32_t ref_dispatch_masked(const uint16_t* x, int64_t ldx, int32_t T, int32_t n
   for (int32_t e = 0; e < L; ++e) {
     masked_m[e] = counts[e] < cap ? counts[e] : cap;
     if (counts[e] > cap) st |= REF_ST_OVERFLOW;
+  }
+  /* [P3 _build_layout] the expanded layout of the slab's real rows: expert e
+   * starts at the previous segment end rounded up to psum_align and ends
+   * masked_m[e] rows later (psum[-1] = 0). */
+  if (psum) {
+    int64_t prev_end = 0;
+    for (int32_t e = 0; e < L; ++e) {
+      int64_t seg_start = align_up(prev_end, psum_align);
+      psum[e] = (int32_t)(seg_start + masked_m[e]);
+      prev_end = psum[e];
+    }
   }
   int32_t G = H / g;
   uint8_t* qrow = (uint8_t*)malloc((size_t)H);

@@ -96,12 +96,15 @@ int32_t ref_dispatch_compact(const uint16_t* x, int64_t ldx, int32_t T, int32_t 
                              int32_t* starts, int32_t* psum, int32_t* total,
                              float* row_weights);
 
-/* [P1][P3] masked dispatch into per-expert slabs [L, cap, H]. */
+/* [P1][P3] masked dispatch into per-expert slabs [L, cap, H]. psum (optional,
+ * [L]) receives the expanded layout of the slab's real rows [P3 _build_layout]:
+ * psum[e] = align(psum[e-1], psum_align) + masked_m[e], psum[-1] = 0. */
 int32_t ref_dispatch_masked(const uint16_t* x, int64_t ldx, int32_t T, int32_t n_live,
                             int32_t H, const int32_t* topk_ids, const float* topk_weights,
                             int32_t K, int32_t L, int32_t cap, int32_t g, int32_t fmt,
                             uint8_t* xq, void* scales, int64_t ld_s, int32_t* masked_m,
-                            int32_t* src2dst, float* row_weights);
+                            int32_t* src2dst, float* row_weights, int32_t* psum,
+                            int32_t psum_align);
 
 /* [P1] combine: fp64 reference out[t,h] = sum_k w*y, plus sum_k |w*y|. */
 void ref_combine_f64(const uint16_t* y, int64_t ldy, const int32_t* src2dst,

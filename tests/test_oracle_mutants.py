@@ -59,6 +59,11 @@ MUTANTS = [
     ("m_indices_tail_filled", "for (int64_t r = 0; r < bound; ++r) m_indices[r] = -1;",
      "for (int64_t r = 0; r < bound; ++r) m_indices[r] = L - 1;",
      ["test_dispatch_compact_invariants_random", "test_dispatch_compact_exhaustive_tiny"]),
+    ("masked_psum_unaligned", "int64_t seg_start = align_up(prev_end, psum_align);",
+     "int64_t seg_start = prev_end;", ["test_dispatch_masked_psum_equals_compact_layout"]),
+    ("masked_psum_unclamped", "psum[e] = (int32_t)(seg_start + masked_m[e]);",
+     "psum[e] = (int32_t)(seg_start + counts[e]);",
+     ["test_dispatch_masked_psum_overflow_follows_masked_m"]),
     ("overflow_flag_off_by_one", "if (counts[e] > cap) st |= REF_ST_OVERFLOW;",
      "if (counts[e] > cap + 1) st |= REF_ST_OVERFLOW;", ["test_dispatch_masked_overflow"]),
     # widened rows: OCP-MX exponent, plain fp32 scales, e8m0 / amax requant, weighted repack
@@ -100,6 +105,8 @@ def run_pin(name):
     params = inspect.signature(fn).parameters
     if "counts" in params:          # parametrised repack pin: run one representative case
         fn(oracle, [3, 0, 5, 1], "bf16")
+    elif "align" in params:
+        fn(oracle, 128)
     elif "fmt" in params:
         fn(oracle, "packed")
     elif "g" in params:

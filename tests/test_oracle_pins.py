@@ -330,7 +330,7 @@ def test_dispatch_compact_exhaustive_tiny(ref):
     assert n > 1000
 
 
-def run_masked(ref, x, ids, w, H, K, L, cap, g, fmt, n_live=None):
+def run_masked(ref, x, ids, w, H, K, L, cap, g, fmt, n_live=None, psum_align=128):
     T = ids.shape[0]
     n_live = T if n_live is None else n_live
     G = H // g
@@ -339,8 +339,10 @@ def run_masked(ref, x, ids, w, H, K, L, cap, g, fmt, n_live=None):
     mm = np.full(L, -5, np.int32)
     s2d = np.full((T, K), -9, np.int32)
     rw = np.full(L * cap, np.nan, np.float32)
-    st = ref.dispatch_masked(x, T, n_live, H, ids, w, K, L, cap, g, fmt, xq, sc, ld, mm, s2d, rw)
-    return dict(st=st, xq=xq, sc=sc, ld=ld, mm=mm, s2d=s2d, rw=rw)
+    ps = np.full(L, -5, np.int32)
+    st = ref.dispatch_masked(x, T, n_live, H, ids, w, K, L, cap, g, fmt, xq, sc, ld, mm, s2d, rw,
+                             psum=ps, psum_align=psum_align)
+    return dict(st=st, xq=xq, sc=sc, ld=ld, mm=mm, s2d=s2d, rw=rw, psum=ps)
 
 
 @pytest.mark.parametrize("fmt", ["packed", "u8"])
@@ -397,6 +399,75 @@ def test_dispatch_masked_overflow(ref):
     r = run_masked(ref, x[:7], ids[:7], w[:7], H, K, L, 6, 128, "u8")
     assert r["st"] & ref.ST_OVERFLOW and r["mm"].tolist() == [6, 0, 0, 0]
     assert r["s2d"][:, 0].tolist() == [0, 1, 2, 3, 4, 5, -1]
+
+
+@pytest.mark.parametrize("align", [128, 16, 1])
+def test_dispatch_masked_psum_equals_compact_layout(ref, align):
+    """Without overflow the masked dispatch's expanded layout (PR #29525
+    _build_layout: segments start at the previous end rounded up to `align`)
+    is the compact layout of PR #33128 with block_e = align, whose starts and
+    psum are pinned on their own (brute force, invariants)."""
+    d = synth.decode(2, T=96)
+    H, K, L, cap, g = 128, 8, 32, 96, 128
+    x = d["x"][:, :H].copy()
+    ids, w = d["topk_ids"], d["topk_weights"]
+    rm = run_masked(ref, x, ids, w, H, K, L, cap, g, "u8", psum_align=align)
+    rc = run_compact(ref, x, ids, w, H, K, L, align, g, "u8")
+    assert rm["st"] == 0
+    assert np.array_equal(rm["psum"], rc["psum"])
+    assert np.array_equal(rm["mm"], rc["counts"])
+
+
+def test_dispatch_masked_psum_overflow_follows_masked_m(ref):
+    """With an overflowing expert, the expanded layout covers only the rows the
+    slab holds (masked_m), so slab -> expand never reads past capacity; the
+    values are the pages' _build_layout of masked_m, computed by hand here."""
+    T, K, L, cap, H = 12, 1, 4, 5, 128
+    ids = np.array([[0]] * 7 + [[2]] * 3 + [[3]] * 2, np.int32)   # counts 7, 0, 3, 2
+    x = synth.to_bf16_bits(np.random.default_rng(1).standard_normal((T, H)).astype(np.float32))
+    w = np.ones((T, K), np.float32)
+    r = run_masked(ref, x, ids, w, H, K, L, cap, 128, "u8", psum_align=8)
+    assert r["st"] & ref.ST_OVERFLOW
+    assert r["mm"].tolist() == [5, 0, 3, 2]
+    # e0 [0, 5), e1 [8, 8), e2 [8, 11), e3 [16, 18)
+    assert r["psum"].tolist() == [5, 8, 11, 18]
+    _, want, _, _ = build_layout([5, 0, 3, 2], 8, 4)
+    assert np.array_equal(r["psum"], want)
+
+
+def test_dispatch_masked_psum_drives_expand_roundtrip(ref):
+    """The psum a masked dispatch reports takes its slab to the expanded layout
+    and back unchanged (PR #29525 _check_expand_roundtrip), with masked_m
+    reproduced and nothing flagged."""
+    d = synth.decode(3, T=64)
+    H, K, L, cap, g, align = 256, 8, 32, 64, 128, 128
+    x = d["x"][:, :H].copy()
+    ids, w = d["topk_ids"], d["topk_weights"]
+    r = run_masked(ref, x, ids, w, H, K, L, cap, g, "packed", psum_align=align)
+    assert r["st"] == 0
+    R = ref.compact_bound(ids.size, L, align)
+    G = H // g
+    exp = np.full((R, H), 0xDD, np.uint8)
+    esc, ld_es = ref.scale_buffer("packed", R, G, fill=0x11)
+    mi = np.full(R, 77, np.int32)
+    st = ref.expand_from_slab(r["xq"], 1, H, r["sc"], r["ld"], r["psum"], L, align, cap, "packed",
+                              g, None, exp, R, esc, ld_es, mi)
+    assert st == 0
+    assert (mi >= 0).sum() == r["mm"].sum()
+    slab2 = np.full_like(r["xq"], 0xEE)
+    ssc2, ld2 = ref.scale_buffer("packed", L * cap, G, blocks=L)
+    mm2 = np.full(L, -1, np.int32)
+    st = ref.expand_to_slab(exp, 1, H, R, esc, ld_es, r["psum"], L, align, cap, "packed", g, slab2,
+                            ssc2, ld2, mm2)
+    assert st == 0
+    assert np.array_equal(mm2, r["mm"])
+    assert np.array_equal(slab2, r["xq"])
+    real = np.zeros(L * cap, bool)
+    for e in range(L):
+        real[e * cap:e * cap + r["mm"][e]] = True
+    got_rows = packed_to_rows(ssc2, L * cap, G, ld2, blocks=L)[real]
+    want_rows = packed_to_rows(r["sc"], L * cap, G, r["ld"], blocks=L)[real]
+    assert np.array_equal(got_rows, want_rows)
 
 
 def test_masked_and_compact_combine_identical(ref):
