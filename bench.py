@@ -250,6 +250,22 @@ def cpu_model():
     return platform.machine()
 
 
+def step_config(world, T=None):
+    """The workload's `config`, identical in both arms (the reference arm runs
+    the same workload on the host, so the GPU arm's L2 flush is named for what
+    it is). T overrides the token count (--tokens)."""
+    c = synth.PREFILL
+    T = c["T"] if T is None else T
+    H, K, E, L, b, g = c["H"], c["K"], c["E"], c["L"], c["block_e"], c["g"]
+    work = WORKLOAD if T == c["T"] else WORKLOAD.replace(f"T={c['T']}", f"T={T}")
+    return {"workload": work, "T": T, "H": H, "K": K, "E": E, "L": L, "block_e": b,
+            "group": g, "scales": "packed UE8M0",
+            "bound_rows": b * (min(T * K, L) + (T * K - min(T * K, L)) // b),
+            "l2": (f"GPU arm: flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write + "
+                   f"{L2_FLUSH_BYTES >> 20} MiB read, outside the events); CPU arm: no flush"),
+            "parallelism": f"replicas x{world} (no collective on the data path)"}
+
+
 # ---------------------------------------------------------------------------
 # reference arm: the oracle as it stands, on host cores
 # ---------------------------------------------------------------------------
@@ -274,8 +290,8 @@ def run_reference(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": statistics.median(secs) * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16->e4m3",
         "data": "synthetic (seeded numpy: Zipf top-8 routing, N(0,1) activations)",
-        "config": {"workload": WORKLOAD, "sample_tokens_per_step": pool.n * pool.tokens,
-                   "l2": "n/a (CPU)"},
+        "config": step_config(args.gpus),
+        "sample_tokens_per_step": pool.n * pool.tokens,
         "cpu_baseline": {"value": v, "unit": UNIT, "cores": pool.n, "kind": "oracle",
                          "sample": sample, "cpu": cpu_model()},
         "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -512,14 +528,11 @@ def run_ours(args, rank, world, local_rank):
         "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16->e4m3 (u8), fp32 accumulate",
         "data": "synthetic (seeded: numpy Zipf top-8 routing and N(0,1) x; torch N(0,1) expert outputs)",
-        "config": {"workload": WORKLOAD, "T": T, "H": H, "K": K, "E": E, "L": L, "block_e": b,
-                   "group": g, "scales": "packed UE8M0", "bound_rows": bound,
-                   "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write + {L2_FLUSH_BYTES >> 20} MiB read, outside the events)",
-                   "parallelism": f"replicas x{world} (no collective on the data path)",
-                   "timing": "per step: L2 flush, then one CUDA-graph replay of the dispatch call and "
-                             "the combine call between two CUDA events (mean of the steps); the "
-                             "per-call split in detail comes from a second loop with an event between "
-                             "the calls"},
+        "config": step_config(world, T),
+        "timing": "per step: L2 flush, then one CUDA-graph replay of the dispatch call and "
+                  "the combine call between two CUDA events (mean of the steps); the "
+                  "per-call split in detail comes from a second loop with an event between "
+                  "the calls",
         "detail": {
             "dispatch": {"us": ms_disp * 1e3, "gbs": disp_gbs, "frac_of_peak": disp_gbs / hbm,
                          "algorithmic_bytes": db, "launches": 2},
@@ -637,9 +650,12 @@ def time_call(fn, flush, reps=40):
 
 
 def other_rows(mp, dev, flush):
-    """Decode (masked) dispatch + slab->expand + combine, MXFP8 live-row quant,
-    requant and expand->slab, each on its own workload (trimmed mean of 40,
-    L2 flushed before each call)."""
+    """The other hot-path rows, each on its own workload (trimmed mean of 40,
+    L2 flushed before each call): the decode chain -- masked dispatch with its
+    expanded-layout psum, slab -> expanded, expanded -> slab, weighted combine
+    from slab rows -- call by call and as one CUDA-graph replay; MXFP8
+    live-row quant; the live-row quantiser on a full batch; requant; and
+    expanded <-> slab on the requant workload."""
     import torch
     hbm, _ = peaks()
     res = {}
@@ -664,19 +680,59 @@ def other_rows(mp, dev, flush):
     kept = int(((dd["topk_ids"] >= 0) & (dd["topk_ids"] < L)).sum())
     live_tok = int((((dd["topk_ids"] >= 0) & (dd["topk_ids"] < L)).any(axis=1)).sum())
 
-    def dec():
-        assert mp.moe_dispatch_masked(x, H, T, None, H, ids, None, K, E, L, cap, g, "packed", xq, sc,
-                                      ld, mm, s2d, None, ws.buf, ws.nbytes, st) == 0
-    us = time_call(dec, flush)
-    nb = live_tok * H * 2 + T * K * 4 + kept * (H + 56) + L * 4 + T * K * 4
-    res["decode_masked_dispatch"] = entry(us, nb)
+    align = c["align"]
+    psum = torch.empty(L, dtype=torch.int32, device=dev)
+    G4 = (H // g + 3) // 4
+    R = mp.moe_compact_bound(T * K, L, align)     # static rows of the expanded layout
+    exp = torch.empty((R, H), dtype=torch.uint8, device=dev)
+    esc, ld_es = mp.scale_tensor("packed", R, H, g, dev)
+    mi = torch.empty(R, dtype=torch.int32, device=dev)
+    slab2 = torch.empty_like(xq)
+    sc2 = torch.empty_like(sc)
+    mm2 = torch.empty_like(mm)
     yslab = torch.randn((L * cap, H), device=dev).to(torch.bfloat16)
     outd = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
 
+    def dec():
+        assert mp.moe_dispatch_masked(x, H, T, None, H, ids, None, K, E, L, cap, g, "packed", xq, sc,
+                                      ld, mm, s2d, None, psum, align, ws.buf, ws.nbytes, st) == 0
+
+    def from_slab():
+        assert mp.moe_expand_from_slab(xq, 1, H, sc, ld, psum, L, align, cap, "packed", g, None, exp,
+                                       R, esc, ld_es, mi, st) == 0
+
+    def to_slab():
+        assert mp.moe_expand_to_slab(exp, 1, H, R, esc, ld_es, psum, L, align, cap, "packed", g,
+                                     slab2, sc2, ld, mm2, st) == 0
+
     def decomb():
         assert mp.moe_combine(yslab, H, L * cap, s2d, w, T, None, K, H, outd, st) == 0
-    us = time_call(decomb, flush)
-    res["decode_combine_from_slab"] = entry(us, kept * H * 2 + T * K * 8 + T * H * 2)
+
+    # x rows of tokens with a local slot and ids read; payload + scale words per
+    # kept slot, masked_m + psum and src2dst written
+    nb_disp = live_tok * H * 2 + T * K * 4 + kept * (H + 4 * G4) + L * 8 + T * K * 4
+    nb_repack = 2 * kept * (H + 4 * G4) + L * 4          # rows and scale words, read + written
+    nb_from = nb_repack + R * 4                           # + m_indices over the expanded rows
+    nb_to = nb_repack + L * 4                             # + masked_m
+    nb_comb = kept * H * 2 + T * K * 8 + T * H * 2
+    res["decode_masked_dispatch"] = entry(time_call(dec, flush), nb_disp)
+    res["decode_slab_to_expand"] = entry(time_call(from_slab, flush), nb_from)
+    res["decode_expand_to_slab"] = entry(time_call(to_slab, flush), nb_to)
+    res["decode_combine_from_slab"] = entry(time_call(decomb, flush), nb_comb)
+    # the whole decode chain, captured once, as one graph replay
+    dec(), from_slab(), to_slab(), decomb()
+    torch.cuda.synchronize()
+    gchain = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gchain):
+        dec()
+        from_slab()
+        to_slab()
+        decomb()
+    res["decode_chain_graph"] = entry(time_call(gchain.replay, flush),
+                                      nb_disp + nb_from + nb_to + nb_comb)
+    res["decode_chain_graph"]["launches"] = 4
+    res["decode_chain_graph"]["expanded_rows"] = R
+    del gchain
 
     # MXFP8 sparse buffer: 112 live rows of 24576
     dm = synth.mxfp8(0)
@@ -801,7 +857,8 @@ def layout_sweep(args):
 
             def masked():
                 assert mp.moe_dispatch_masked(x, H, T, None, H, ids, None, K, E, L, cap, g, "packed",
-                                              xqm, scm, ldm, mm, s2d, None, ws.buf, ws.nbytes, st) == 0
+                                              xqm, scm, ldm, mm, s2d, None, None, 128, ws.buf,
+                                              ws.nbytes, st) == 0
             uc, um = time_call(compact, flush), time_call(masked, flush)
             torch.cuda.synchronize()
             assert mp.moe_status_sync(st) == 0

@@ -216,7 +216,7 @@ size_t moe_workspace_bytes(int32_t T, int32_t K, int32_t L) {
   // (a preference that no chain meets falls back to the shortest chain under
   // the hard limit, which can be the larger table)
   int64_t nc = 0;
-  for (int64_t pref : {(int64_t)MOEPERM_ROUTE_TABLE_PREF_SMALL, (int64_t)MOEPERM_ROUTE_TABLE_PREF}) {
+  for (int64_t pref : {kRouteTablePrefSmall, kRouteTablePref}) {
     const RouteGeom geom = route_geometry(A, L, pref);
     if (geom.S == 0) return 0;
     if (geom.nchunks > nc) nc = geom.nchunks;
@@ -252,8 +252,8 @@ moe_status_t moe_dispatch_masked(
     const int32_t* topk_ids, const float* topk_weights, int32_t K, int32_t E, int32_t L,
     int32_t cap, int32_t g, moe_scale_fmt_t fmt,
     void* xq, void* scales, int64_t ld_s, int32_t* masked_m, int32_t* src2dst,
-    float* row_weights, void* workspace, size_t workspace_bytes, int32_t* d_status,
-    moe_stream_t stream) {
+    float* row_weights, int32_t* psum, int32_t psum_align, void* workspace,
+    size_t workspace_bytes, int32_t* d_status, moe_stream_t stream) {
   DispatchCommon c{x, ldx, T, d_num_tokens, H, topk_ids, topk_weights, K, E, L, g, (int)fmt,
                    xq, scales, ld_s, src2dst, row_weights, workspace, workspace_bytes};
   moe_status_t st = check_common(c);
@@ -261,8 +261,11 @@ moe_status_t moe_dispatch_masked(
   if (cap < 1 || (int64_t)L * cap >= (int64_t(1) << 31)) return MOE_ERR_INVALID_ARG;
   if (!masked_m || !xq || !aligned16(xq) || !scales || !aligned16(scales)) return MOE_ERR_INVALID_ARG;
   if (!ld_ok(fmt, ld_s, cap, H / g)) return MOE_ERR_INVALID_ARG;
-  return run_dispatch(c, kModeMasked, 1, cap, nullptr, 0, nullptr, nullptr, nullptr, nullptr,
-                      masked_m, d_status, reinterpret_cast<cudaStream_t>(stream));
+  // the expanded layout of the slab rows ends below align * L + L * cap
+  if (psum && (psum_align < 1 || (int64_t)L * (psum_align + (int64_t)cap) >= (int64_t(1) << 31)))
+    return MOE_ERR_INVALID_ARG;
+  return run_dispatch(c, kModeMasked, psum ? psum_align : 1, cap, nullptr, 0, nullptr, nullptr,
+                      psum, nullptr, masked_m, d_status, reinterpret_cast<cudaStream_t>(stream));
 }
 
 moe_status_t moe_quant_group(const void* x, int64_t ldx, int32_t T_cap, const int32_t* d_num_live,

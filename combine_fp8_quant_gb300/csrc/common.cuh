@@ -167,25 +167,17 @@ __device__ __forceinline__ void pdl_wait_primary() {
 }
 
 // Bulk (TMA) copy of `bytes` from shared memory to global memory, tracked in
-// the issuing thread's bulk groups. Both addresses 16-byte aligned, bytes a
+// the issuing thread's bulk groups, with an L2 cache policy (from
+// createpolicy) on the written lines. Both addresses 16-byte aligned, bytes a
 // multiple of 16.
-__device__ __forceinline__ void bulk_store_s2g(void* gdst, uint32_t ssrc, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
-               ::"l"(gdst), "r"(ssrc), "r"(bytes)
-               : "memory");
-}
-// Same, with an L2 cache policy (from createpolicy) on the written lines.
 __device__ __forceinline__ void bulk_store_s2g_hint(void* gdst, uint32_t ssrc, uint32_t bytes,
                                                     uint64_t policy) {
   asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;"
                ::"l"(gdst), "r"(ssrc), "r"(bytes), "l"(policy)
                : "memory");
 }
-// Bulk (TMA) prefetch of `bytes` of global memory into L2 (16-byte aligned
-// address, bytes a multiple of 16); nothing waits for it.
-__device__ __forceinline__ void bulk_prefetch_l2(const void* g, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(g), "r"(bytes) : "memory");
-}
+// Bulk (TMA) prefetch of `bytes` of global memory into L2 with an L2 cache
+// policy (16-byte aligned address, bytes a multiple of 16); nothing waits for it.
 __device__ __forceinline__ void bulk_prefetch_l2_hint(const void* g, uint32_t bytes, uint64_t policy) {
   asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;"
                ::"l"(g), "r"(bytes), "l"(policy)
@@ -246,5 +238,41 @@ inline cudaError_t occupancy(Kern kernel, int threads, size_t smem, int* per_sm)
 }
 
 __device__ __forceinline__ int64_t align_up64(int64_t c, int64_t b) { return (c + b - 1) / b * b; }
+
+// Segment starts of a layout whose segments are padded to multiples of b, in
+// expert order: st[e] = sum over e' < e of align(min(cnt[e'], clamp), b), for
+// e < L (PR #33128 compact starts; PR #29525 _build_layout starts). One CTA:
+// thread i owns a contiguous run of experts, a warp scan and a scan over the
+// warp totals join the runs. Returns the total in every thread. Every thread
+// of the CTA must call it (blockDim.x a multiple of 32); it begins reading cnt
+// and ends with a barrier. s_wsum: at least blockDim.x / 32 ints of shared memory.
+__device__ __forceinline__ int aligned_starts(const int32_t* cnt, int32_t* st, int L, int b,
+                                              int clamp, int32_t* s_wsum) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, bd = blockDim.x;
+  const int per = (L + bd - 1) / bd;
+  const int lo = min(tid * per, L), hi = min(lo + per, L);
+  int local = 0;
+  for (int e = lo; e < hi; ++e) local += (min(cnt[e], clamp) + b - 1) / b * b;
+  int incl = local;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int nb = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += nb;
+  }
+  if (lane == 31) s_wsum[warp] = incl;
+  __syncthreads();
+  int wbase = 0, total = 0;
+  for (int w = 0; w < (bd >> 5); ++w) {
+    if (w < warp) wbase += s_wsum[w];
+    total += s_wsum[w];
+  }
+  int run = wbase + incl - local;
+  for (int e = lo; e < hi; ++e) {
+    st[e] = run;
+    run += (min(cnt[e], clamp) + b - 1) / b * b;
+  }
+  __syncthreads();
+  return total;
+}
 
 }  // namespace moeperm

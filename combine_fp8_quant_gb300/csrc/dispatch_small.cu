@@ -23,6 +23,8 @@
 //   5. quantise its tokens (a 16-element chunk pair per thread per pass,
 //      xor-shuffle group max, exponent from the float's bits, hardware e4m3
 //      converts) and store each 16-byte vector to every destination row.
+#include <climits>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "scales.cuh"
@@ -114,32 +116,8 @@ __global__ void __launch_bounds__(kThreads) dispatch_small_kernel(ScatterArgs p)
   }
   __syncthreads();
   if (p.mode == kModeCompact) {
-    const int b = p.block_e;
-    const int per = (L + kThreads - 1) / kThreads;
-    const int lo = min(tid * per, L), hi = min(lo + per, L);
-    int local = 0;
-    for (int e = lo; e < hi; ++e) local += (ps[e] + b - 1) / b * b;
-    int incl = local;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int nb = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += nb;
-    }
-    if (lane == 31) s_wsum[warp] = incl;
-    __syncthreads();
-    int wbase = 0, total = 0;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      if (w < warp) wbase += s_wsum[w];
-      total += s_wsum[w];
-    }
-    int run = wbase + incl - local;
-    for (int e = lo; e < hi; ++e) {
-      const int cnt = ps[e];
-      st[e] = run;
-      ps[e] = run + cnt;
-      run += (cnt + b - 1) / b * b;
-    }
+    const int total = aligned_starts(ps, st, L, p.block_e, INT_MAX, s_wsum);
+    for (int e = tid; e < L; e += kThreads) ps[e] += st[e];  // count -> psum
     if (blockIdx.x == 0 && tid == 0) *p.total = total;
     __syncthreads();
     if (blockIdx.x == 0)
@@ -159,13 +137,18 @@ __global__ void __launch_bounds__(kThreads) dispatch_small_kernel(ScatterArgs p)
         p.m_indices[rr] = (rr < ps[lo2]) ? lo2 : -1;
       }
   } else {
+    // masked: slab rows need no start, so st takes the expanded-layout starts
+    // of the slab's real rows when psum is asked for (PR #29525 _build_layout)
     bool overflow = false;
     for (int e = tid; e < L; e += kThreads) {
       if (blockIdx.x == 0) p.masked_m[e] = min(ps[e], p.cap);
       if (ps[e] > p.cap) overflow = true;
-      st[e] = 0;
     }
     if (overflow && blockIdx.x == 0) set_status(p.status, kStOverflow);
+    if (p.psum != nullptr && blockIdx.x == 0) {  // uniform over the CTA
+      aligned_starts(ps, st, L, p.block_e, p.cap, s_wsum);
+      for (int e = tid; e < L; e += kThreads) p.psum[e] = st[e] + min(ps[e], p.cap);
+    }
     __syncthreads();
   }
 

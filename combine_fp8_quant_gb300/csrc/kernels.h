@@ -42,16 +42,12 @@ struct RouteGeom {
 // per token, so its loop is latency-bound and the residency that a small
 // table leaves (4 rather than 3 CTAs per SM at H = 7168) decides; with more
 // experts the loop is bandwidth-bound and the shorter chain wins.
-#ifndef MOEPERM_ROUTE_TABLE_PREF
-#define MOEPERM_ROUTE_TABLE_PREF 8192
-#endif
-#ifndef MOEPERM_ROUTE_TABLE_PREF_SMALL
-#define MOEPERM_ROUTE_TABLE_PREF_SMALL 2048
-#endif
+constexpr int64_t kRouteTablePref = 8192;
+constexpr int64_t kRouteTablePrefSmall = 2048;
 constexpr int kNarrowRow = 4096;   // H below this: the small-table preference
 constexpr int kFewExperts = 128;   // L up to this: the small-table preference
 inline int64_t route_table_pref(int H, int L) {
-  return (H < kNarrowRow || L <= kFewExperts) ? MOEPERM_ROUTE_TABLE_PREF_SMALL : MOEPERM_ROUTE_TABLE_PREF;
+  return (H < kNarrowRow || L <= kFewExperts) ? kRouteTablePrefSmall : kRouteTablePref;
 }
 RouteGeom route_geometry(int64_t A, int L, int64_t table_pref);
 cudaError_t launch_route_plan(const RoutePlanArgs& a, const RouteGeom& g, cudaStream_t s);
@@ -98,10 +94,7 @@ cudaError_t launch_quant_scatter(const ScatterArgs& a, int g, int fmt, int num_s
 // ranks all slots itself; no chunk table, no route-plan launch. Measured on
 // GB300 (H = 7168, top-8): faster than the two-launch plan up to 2048 slots,
 // equal at 2048, slower at 4096 (the redundant ranking grows with T*K).
-#ifndef MOEPERM_SMALL_SLOTS
-#define MOEPERM_SMALL_SLOTS 2048
-#endif
-constexpr int64_t kSmallSlots = MOEPERM_SMALL_SLOTS;
+constexpr int64_t kSmallSlots = 2048;
 // The one-launch kernel ranks at most 8 warps x 32 lanes x 16 steps slots.
 constexpr int64_t kSmallSlotsMax = 4096;
 static_assert(kSmallSlots <= kSmallSlotsMax, "the one-launch dispatch ranks at most 4096 slots");

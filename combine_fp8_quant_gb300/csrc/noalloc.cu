@@ -1,23 +1,31 @@
 // noalloc.cu -- moe_dispatch_compact_noalloc: the compact dispatch for callers
 // that cannot allocate device memory.
 //
-// Some callers cannot call cudaMalloc or any allocating routine. Examples:
-//   - code that runs while a CUDA graph is being captured, where allocation is
-//     not allowed;
-//   - plugins hosted by an engine that owns every device allocation and hands
-//     out only inputs and outputs;
-//   - latency-critical serving loops that forbid allocation after start-up.
-// moe_dispatch_compact needs a small scratch workspace (the per-chunk expert
-// table), which such a caller would otherwise have to allocate. This variant keeps that scratch in one file-scope device array of
-// fixed size instead. Every GPU that loads the library holds the array until
-// the process exits.
+// Some callers cannot call cudaMalloc or any other allocating routine: a
+// plugin inside a host engine that owns every device allocation and hands the
+// plugin only its inputs and outputs, a serving loop that forbids allocation
+// after start-up so that its memory footprint stays fixed, or a runtime with
+// a fixed device-memory budget. moe_dispatch_compact needs a small scratch
+// workspace (a token counter, and the per-chunk expert table on the
+// two-launch path), which such a caller would otherwise have to allocate.
+// This variant keeps that scratch in one file-scope device array of fixed
+// size instead. Every GPU that loads the library holds the array until the
+// process exits.
 //
-// The host cannot use the array's name as a device address: in host code the
-// name is only a host-side stand-in. The address is therefore looked up once
-// per device with cudaGetSymbolAddress, on the first call made with that
-// device current, and cached. Calls after that only enqueue a memset of the
-// used part of the array (so no call can see a previous call's table) and the
-// two dispatch kernels.
+// In host code the array's name is only a host-side stand-in, not a device
+// address: handing it to a kernel would fault or silently use the wrong
+// memory. The device address is therefore looked up with
+// cudaGetSymbolAddress, with the device current, on the first call in each
+// CUDA context (normally once per device: the primary context), and cached
+// under the context's unique id. A context created again after
+// cudaDeviceReset has a new id, so the address is looked up again there
+// rather than reused.
+//
+// Nothing in the array has to start at zero: the route plan writes every
+// chunk-table word before the scatter reads it and resets the token counter
+// itself, so a call neither clears the array nor depends on what the previous
+// call left in it.
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -27,28 +35,81 @@
 
 namespace {
 
-// 64 KiB chunk table plus the 256-byte reserved header of the workspace layout.
+// The largest workspace moe_workspace_bytes reports: a 64 KiB chunk table
+// plus the 256-byte reserved header.
 constexpr size_t kNoAllocScratchBytes = 64 * 1024 + 256;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-constexpr int kMaxDevices = 128;
-std::mutex g_setup_mutex;
-void* g_scratch_addr[kMaxDevices] = {nullptr};
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
 
-// Device address of the scratch array on the current device (set-up on first use).
-cudaError_t scratch_address(void** out) {
-  int dev = -1;
-  cudaError_t err = cudaGetDevice(&dev);
+struct ScratchEntry {
+  unsigned long long ctx_id;
+  void* addr;
+};
+constexpr int kMaxEntries = 64;
+std::mutex g_setup_mutex;
+ScratchEntry g_entries[kMaxEntries];
+int g_nentries = 0;
+int g_next = 0;  // entry replaced when the table is full
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
+
+// Driver entry points for the current context and its id, looked up through
+// the runtime (the library does not link the driver library directly).
+cudaError_t driver_entry_points() {
+  if (g_ctx_get_current != nullptr && g_ctx_get_id != nullptr) return cudaSuccess;
+  void* f1 = nullptr;
+  void* f2 = nullptr;
+  cudaDriverEntryPointQueryResult q1 = cudaDriverEntryPointSymbolNotFound;
+  cudaDriverEntryPointQueryResult q2 = cudaDriverEntryPointSymbolNotFound;
+  cudaError_t err = cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 12000,
+                                                     cudaEnableDefault, &q1);
   if (err != cudaSuccess) return err;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  err = cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2);
+  if (err != cudaSuccess) return err;
+  if (q1 != cudaDriverEntryPointSuccess || q2 != cudaDriverEntryPointSuccess || !f1 || !f2)
+    return cudaErrorSymbolNotFound;
+  g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(f1);
+  g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(f2);
+  return cudaSuccess;
+}
+
+// Unique id of the context current on this thread (0 when none is).
+cudaError_t current_context_id(unsigned long long* id) {
+  *id = 0;
+  CUcontext ctx = nullptr;
+  if (g_ctx_get_current(&ctx) != CUDA_SUCCESS) return cudaErrorUnknown;
+  if (ctx == nullptr) return cudaSuccess;
+  return g_ctx_get_id(ctx, id) == CUDA_SUCCESS ? cudaSuccess : cudaErrorUnknown;
+}
+
+// Device address of the scratch array in the current context; the first call
+// in a context looks it up (which also initialises the device's primary
+// context if no context is current yet).
+cudaError_t scratch_address(void** out) {
   std::lock_guard<std::mutex> lock(g_setup_mutex);
-  if (g_scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
-    err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (err != cudaSuccess) return err;
-    g_scratch_addr[dev] = p;
+  cudaError_t err = driver_entry_points();
+  if (err != cudaSuccess) return err;
+  unsigned long long id = 0;
+  err = current_context_id(&id);
+  if (err != cudaSuccess) return err;
+  if (id != 0)
+    for (int i = 0; i < g_nentries; ++i)
+      if (g_entries[i].ctx_id == id) {
+        *out = g_entries[i].addr;
+        return cudaSuccess;
+      }
+  void* p = nullptr;
+  err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  if (err != cudaSuccess) return err;
+  err = current_context_id(&id);
+  if (err != cudaSuccess) return err;
+  if (id != 0) {
+    int slot = g_nentries < kMaxEntries ? g_nentries++ : (g_next++ % kMaxEntries);
+    g_entries[slot] = ScratchEntry{id, p};
   }
-  *out = g_scratch_addr[dev];
+  *out = p;
   return cudaSuccess;
 }
 
@@ -65,9 +126,7 @@ extern "C" moe_status_t moe_dispatch_compact_noalloc(
   if (need == 0 || need > kNoAllocScratchBytes) return MOE_ERR_INVALID_ARG;
   void* scratch = nullptr;
   if (scratch_address(&scratch) != cudaSuccess) return MOE_ERR_CUDA;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // The array keeps the previous call's contents: clear the part this call uses.
-  if (cudaMemsetAsync(scratch, 0, need, s) != cudaSuccess) return MOE_ERR_CUDA;
+  // moe_dispatch_compact validates every argument before it enqueues anything.
   return moe_dispatch_compact(x, ldx, T, d_num_tokens, H, topk_ids, topk_weights, K, E, L,
                               block_e, g, fmt, xq, scales, ld_s, m_indices, bound, src2dst,
                               counts, starts, psum, total, row_weights, scratch,

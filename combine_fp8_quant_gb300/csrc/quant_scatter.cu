@@ -51,6 +51,8 @@
 //   for the packed UE8M0 layout exactly one 32-bit word per warp (4 groups of
 //   128) per destination, the K destinations written from K lanes at once
 //   (scales.cuh).
+#include <climits>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "scales.cuh"
@@ -59,59 +61,27 @@ namespace moeperm {
 
 namespace {
 
-#ifndef MOEPERM_SCATTER_STAGES
-#define MOEPERM_SCATTER_STAGES 4
-#endif
-#ifndef MOEPERM_SCATTER_PRE
-#define MOEPERM_SCATTER_PRE 2
-#endif
-// Rows up to this width take one 16-element chunk per thread (twice the
-// threads per CTA); wider rows take two.
-#ifndef MOEPERM_SCATTER_CPT1_MAX_H
-#define MOEPERM_SCATTER_CPT1_MAX_H 5120
-#endif
-static_assert(MOEPERM_SCATTER_CPT1_MAX_H <= 16384, "one chunk per thread covers at most 1024 x 16 elements");
-#ifndef MOEPERM_SCATTER_MIN_BLOCKS
-#define MOEPERM_SCATTER_MIN_BLOCKS 1
-#endif
-// Tokens ahead of the register prefetch whose x rows thread 0 prefetches
-// into L2 with a bulk prefetch (0: none), and L2 policies for those lines
-// (evict_last) and for the payload rows written (evict_first).
-#ifndef MOEPERM_SCATTER_L2PF
-#define MOEPERM_SCATTER_L2PF 0
-#endif
-#ifndef MOEPERM_SCATTER_PF_HINT
-#define MOEPERM_SCATTER_PF_HINT 0
-#endif
-#ifndef MOEPERM_SCATTER_ST_HINT
-#define MOEPERM_SCATTER_ST_HINT 1
-#endif
-// Tokens after the early-staged ones whose x rows are bulk-prefetched into L2
-// before the wait on the route plan (staged path; 0: none).
-#ifndef MOEPERM_SCATTER_PREFETCH_EARLY
-#define MOEPERM_SCATTER_PREFETCH_EARLY 2
-#endif
-// Direct stores instead of staging when few slots per token are kept: 1 =
-// always, 0 = never, -1 = when the expected kept slots per token, K * L / E
-// (uniform routing), are at most MOEPERM_SCATTER_DIRECT_FANOUT.
-#ifndef MOEPERM_SCATTER_DIRECT
-#define MOEPERM_SCATTER_DIRECT -1
-#endif
-#ifndef MOEPERM_SCATTER_DIRECT_FANOUT
-#define MOEPERM_SCATTER_DIRECT_FANOUT 3
-#endif
-// Direct mode with rows of two chunks per thread: tokens taken from a counter
-// in the workspace (1), so every CTA ends with about the same number of tokens
-// that have a kept slot, or each CTA's strided tokens (0). Measured on GB300,
-// T = 8192, H = 7168, 32 of 256 experts local: 43.7 -> 39.4 us.
-#ifndef MOEPERM_SCATTER_DIRECT_QUEUE
-#define MOEPERM_SCATTER_DIRECT_QUEUE 1
-#endif
 // Largest staging ring (rows in flight to the bulk-copy engine) and number of
 // tokens quantised before the wait on the route plan; the launch lowers both
-// when shared memory is short (large H with a large chunk table).
-constexpr int kStages = MOEPERM_SCATTER_STAGES;
-constexpr int kPre = MOEPERM_SCATTER_PRE < kStages ? MOEPERM_SCATTER_PRE : kStages;
+// when shared memory is short (large H with a large chunk table). Measured on
+// the prefill workload: 4 buffers / 2 early tokens 102.7-103.0 us, 3 / 2
+// 105.6, 5 / 2 106.7 (5 buffers drop to 3 CTAs per SM), 6 / 4 104.2.
+constexpr int kStages = 4;
+constexpr int kPre = 2;
+// Rows up to this width take one 16-element chunk per thread (twice the
+// threads per CTA); wider rows take two (H = 2048: 59 against 67 us; H = 7168:
+// 105 against 109 us the other way round).
+constexpr int kCpt1MaxH = 5120;
+static_assert(kCpt1MaxH <= 16384, "one chunk per thread covers at most 1024 x 16 elements");
+// Tokens after the early-staged ones whose x rows are bulk-prefetched into L2
+// (evict_last) before the wait on the route plan, while HBM is mostly idle
+// (staged path; whole step 266.8 -> 265.6 us with 2).
+constexpr int kPrefetchEarly = 2;
+// Direct stores instead of staging when the expected kept slots per token,
+// K * L / E (uniform routing), are at most this many (staged -> direct at
+// T = 8192, H = 7168: f = 1 47.1 -> 43.0 us, f = 3 62.9 -> 61.5, f = 4
+// 69.1 -> 72.0).
+constexpr int kDirectFanout = 3;
 static_assert(kStages >= 2 && kStages <= 6, "staging ring of 2 to 6 rows");
 
 // Dynamic shared memory: [table nchunks*L | starts L | psum L | rows ntok*K |
@@ -199,32 +169,9 @@ __device__ void layout_prologue(const ScatterArgs& p, int32_t* tbl, int32_t* st,
   }
   __syncthreads();
   if (p.mode == kModeCompact) {
-    // exclusive scan of align(count) over experts; thread i owns a contiguous run
-    const int b = p.block_e;
-    const int per = (L + bd - 1) / bd;
-    const int lo = min(tid * per, L), hi = min(lo + per, L);
-    int local = 0;
-    for (int e = lo; e < hi; ++e) local += (ps[e] + b - 1) / b * b;
-    int incl = local;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int nb = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += nb;
-    }
-    if (lane == 31) s_wsum[warp] = incl;
-    __syncthreads();
-    int wbase = 0, total = 0;
-    for (int w = 0; w < (bd >> 5); ++w) {
-      if (w < warp) wbase += s_wsum[w];
-      total += s_wsum[w];
-    }
-    int run = wbase + incl - local;
-    for (int e = lo; e < hi; ++e) {
-      const int cnt = ps[e];
-      st[e] = run;
-      ps[e] = run + cnt;
-      run += (cnt + b - 1) / b * b;
-    }
+    // segment starts: exclusive scan of align(count) over experts
+    const int total = aligned_starts(ps, st, L, p.block_e, INT_MAX, s_wsum);
+    for (int e = tid; e < L; e += bd) ps[e] += st[e];  // count -> psum
     if (blockIdx.x == 0 && tid == 0) *p.total = total;
     __syncthreads();
     if (blockIdx.x == 0) {
@@ -235,14 +182,20 @@ __device__ void layout_prologue(const ScatterArgs& p, int32_t* tbl, int32_t* st,
       }
     }
   } else {
+    // masked: masked_m = min(count, cap) and the overflow flag; st is free
+    // here (slab rows need no start) and takes the expanded-layout starts of
+    // the slab's real rows when psum is asked for (PR #29525 _build_layout)
     bool overflow = false;
     for (int e = tid; e < L; e += bd) {
       const int cnt = ps[e];
       if (blockIdx.x == 0) p.masked_m[e] = min(cnt, p.cap);
       if (cnt > p.cap) overflow = true;
-      st[e] = 0;
     }
     if (overflow && blockIdx.x == 0) set_status(p.status, kStOverflow);
+    if (p.psum != nullptr && blockIdx.x == 0) {  // uniform over the CTA
+      aligned_starts(ps, st, L, p.block_e, p.cap, s_wsum);
+      for (int e = tid; e < L; e += bd) p.psum[e] = st[e] + min(ps[e], p.cap);
+    }
     __syncthreads();
   }
 }
@@ -298,7 +251,7 @@ __device__ __forceinline__ int slot_row(const ScatterArgs& p, const int32_t* tbl
 }
 
 template <int GSZ, int FMT, int CPT>
-__global__ void __launch_bounds__(1024, MOEPERM_SCATTER_MIN_BLOCKS) quant_scatter_kernel(ScatterArgs p) {
+__global__ void __launch_bounds__(1024, 1) quant_scatter_kernel(ScatterArgs p) {
   extern __shared__ int32_t sm[];
   __shared__ int32_t s_wsum[32];
   __shared__ int32_t s_nlist;
@@ -340,9 +293,9 @@ __global__ void __launch_bounds__(1024, MOEPERM_SCATTER_MIN_BLOCKS) quant_scatte
     // route plan still runs (their rows are not known yet); their scales wait
     // in shared memory.
     npre = p.direct ? 0 : (ntok < p.pre ? ntok : p.pre);
-    if (MOEPERM_SCATTER_PREFETCH_EARLY > 0 && !p.direct && tid == 0) {
+    if (kPrefetchEarly > 0 && !p.direct && tid == 0) {
       const uint64_t pol = l2_policy_evict_last();
-      for (int j = npre; j < ntok && j < npre + MOEPERM_SCATTER_PREFETCH_EARLY; ++j)
+      for (int j = npre; j < ntok && j < npre + kPrefetchEarly; ++j)
         bulk_prefetch_l2_hint(p.x + (int64_t)(blockIdx.x + j * gridDim.x) * p.ldx, (uint32_t)(2 * H), pol);
     }
     for (int j = 0; j < npre; ++j) {
@@ -586,24 +539,14 @@ __global__ void __launch_bounds__(1024, MOEPERM_SCATTER_MIN_BLOCKS) quant_scatte
   // scales stored here.
   const uint32_t stage_s = (uint32_t)__cvta_generic_to_shared(stage);
   int ident_row[1];
-  uint64_t pf_policy = 0, st_policy = 0;
-  if (MOEPERM_SCATTER_PF_HINT) pf_policy = l2_policy_evict_last();
-  if (MOEPERM_SCATTER_ST_HINT) st_policy = l2_policy_evict_first();
-  auto prefetch_x = [&](int m) {  // list entry m, if it is one the loop will load
-    if (MOEPERM_SCATTER_L2PF > 0 && tid == 0 && m >= npre && m < nlist) {
-      const int itp = identity ? m : list_s[m];
-      const uint16_t* src = p.x + (int64_t)(blockIdx.x + itp * gridDim.x) * p.ldx;
-      if (MOEPERM_SCATTER_PF_HINT) bulk_prefetch_l2_hint(src, (uint32_t)(2 * H), pf_policy);
-      else bulk_prefetch_l2(src, (uint32_t)(2 * H));
-    }
-  };
-  for (int m = npre; m <= MOEPERM_SCATTER_L2PF; ++m) prefetch_x(m);
+  // evict_first on the payload rows: nothing here reads them back (prefill
+  // 103.1-103.4 -> 103.1-103.3 us, 32 of 256 experts local 47.1 -> 45.1 us)
+  const uint64_t st_policy = l2_policy_evict_first();
   for (int n = 0; n < nlist; ++n) {
     const int it = identity ? n : list_s[n];
     const int t = blockIdx.x + it * gridDim.x;
     const bool staged = n < npre;  // the staged tokens are list entries 0 .. npre-1
     const bool fetch = n + 1 >= npre;
-    prefetch_x(n + 1 + MOEPERM_SCATTER_L2PF);
     uint4 vn[CPT][2];
     if (fetch) {
       const int itn = n + 1 < nlist ? (identity ? n + 1 : list_s[n + 1]) : -1;
@@ -645,10 +588,7 @@ __global__ void __launch_bounds__(1024, MOEPERM_SCATTER_MIN_BLOCKS) quant_scatte
       for (int k = 0; k < nslots; ++k) {
         const int row = rows[k];
         if (row < 0) continue;
-        if (MOEPERM_SCATTER_ST_HINT)
-          bulk_store_s2g_hint(p.xq + (int64_t)row * H, stage_s + (uint32_t)(buf * H), (uint32_t)H, st_policy);
-        else
-          bulk_store_s2g(p.xq + (int64_t)row * H, stage_s + (uint32_t)(buf * H), (uint32_t)H);
+        bulk_store_s2g_hint(p.xq + (int64_t)row * H, stage_s + (uint32_t)(buf * H), (uint32_t)H, st_policy);
       }
       bulk_commit();
     }
@@ -694,8 +634,7 @@ cudaError_t launch_one(const ScatterArgs& a0, int num_sms, bool pdl, cudaStream_
   ScatterArgs a = a0;
   a.direct = 0;
   if (a.mode != kModeIdentity) {
-    if (MOEPERM_SCATTER_DIRECT >= 0) a.direct = MOEPERM_SCATTER_DIRECT;
-    else a.direct = (int64_t)a.K * a.L <= (int64_t)MOEPERM_SCATTER_DIRECT_FANOUT * a.E ? 1 : 0;
+    a.direct = (int64_t)a.K * a.L <= (int64_t)kDirectFanout * a.E ? 1 : 0;
   }
   auto fit = [&](int64_t ntok) {
     a.stages = a.direct ? 0 : kStages;
@@ -709,8 +648,7 @@ cudaError_t launch_one(const ScatterArgs& a0, int num_sms, bool pdl, cudaStream_
   // (wide rows only: at two chunks per thread a token is enough work to hide
   // the per-token barrier; with narrow rows the static assignment is faster,
   // T = 16384, H = 2048: 31.2 against 36.1 us)
-  a.dyn = (MOEPERM_SCATTER_DIRECT_QUEUE && CPT == 2 && a.direct && a.queue != nullptr && a.K <= 32 &&
-           bd + 32 <= 1024) ? 1 : 0;
+  a.dyn = (CPT == 2 && a.direct && a.queue != nullptr && a.K <= 32 && bd + 32 <= 1024) ? 1 : 0;
   const int block = bd + (a.dyn ? 32 : 0);
   fit(16);
   int per_sm = 0;
@@ -759,7 +697,7 @@ cudaError_t launch_quant_scatter(const ScatterArgs& a, int g, int fmt, int num_s
   // Narrow rows: one chunk per thread, so a CTA still has enough threads to
   // keep loads in flight (measured on GB300: H = 2048 dispatch 67 -> 59 us;
   // at H = 7168 two chunks per thread are faster, 105 against 109 us).
-  if (a.H <= MOEPERM_SCATTER_CPT1_MAX_H) return launch_cpt<1>(a, g, fmt, num_sms, after_route_plan, s);
+  if (a.H <= kCpt1MaxH) return launch_cpt<1>(a, g, fmt, num_sms, after_route_plan, s);
   return launch_cpt<2>(a, g, fmt, num_sms, after_route_plan, s);
 }
 

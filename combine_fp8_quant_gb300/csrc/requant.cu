@@ -87,13 +87,8 @@ __device__ __forceinline__ float reduce_e8m0(const uint8_t* b, int n, float* s_r
 // Rows are processed one per warp: a lane issues kPass 16-byte loads of its
 // row before the first conversion of each pass (8: a 7 KB row in two passes,
 // within 80 registers so that 3 CTAs fit per SM).
-#ifndef MOEPERM_REQUANT_PASS
-#define MOEPERM_REQUANT_PASS 8
-#endif
-#ifndef MOEPERM_REQUANT_MIN_BLOCKS
-#define MOEPERM_REQUANT_MIN_BLOCKS 3
-#endif
-constexpr int kPass = MOEPERM_REQUANT_PASS;
+constexpr int kPass = 8;
+constexpr int kMinBlocks = 3;  // CTAs per SM the rescale kernel is compiled for (80 registers)
 
 // amax mode, launch 1: ws[t] = fl32(s[t] * max_h |decode(q[t, h])|)
 template <int SFMT>
@@ -125,7 +120,7 @@ __global__ void __launch_bounds__(kThreads) requant_rowmax_kernel(RequantArgs p)
 }
 
 template <int SFMT, int MODE>
-__global__ void __launch_bounds__(kThreads, MOEPERM_REQUANT_MIN_BLOCKS) requant_kernel(RequantArgs p) {
+__global__ void __launch_bounds__(kThreads, kMinBlocks) requant_kernel(RequantArgs p) {
   __shared__ float s_red[kThreads / 32];
   const int lane = threadIdx.x & 31, tid = threadIdx.x;
   const int gwarp = (int)((blockIdx.x * kThreads + threadIdx.x) >> 5);

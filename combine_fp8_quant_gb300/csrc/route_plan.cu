@@ -31,10 +31,6 @@ namespace moeperm {
 namespace {
 
 constexpr int kGroup = 8;  // steps whose peer masks are formed together
-// Peer masks from __match_any_sync (1) or from one ballot per expert-id bit (0).
-#ifndef MOEPERM_ROUTE_MATCH
-#define MOEPERM_ROUTE_MATCH 1
-#endif
 // Per-warp histograms (warps x local experts, int32) a CTA may hold: 48 KiB.
 constexpr int kHistInts = 12288;
 // Warps a CTA may have for chain length S: the S = 64 kernel keeps its 64
@@ -63,14 +59,12 @@ __global__ void __launch_bounds__(32 * max_warps_for(S)) route_plan_kernel(Route
   }
   __syncthreads();
 
-  // Lanes with the same expert ("peers"): one match over the warp, or one
-  // ballot per bit of the expert id (a lane keeps the lanes that agree with it
-  // on every bit). The masks of 8 steps are formed first (independent), then
+  // Lanes with the same expert ("peers"): one match over the warp (one
+  // ballot per bit of the expert id measured the same). The masks of 8 steps are formed first (independent), then
   // the per-warp counters are advanced step by step in order, which fixes a
   // stable rank.
   int32_t* myhw = smem + warp * L;
   const unsigned lt_mask = (1u << lane) - 1u;
-  const int nbits = (L > 1) ? 32 - __clz(L - 1) : 0;
 #pragma unroll
   for (int i0 = 0; i0 < S; i0 += kGroup) {
     unsigned peers[kGroup];
@@ -80,17 +74,7 @@ __global__ void __launch_bounds__(32 * max_warps_for(S)) route_plan_kernel(Route
       int e = v[i0 + j];
       if (e < 0 || e >= L) e = -1;
       v[i0 + j] = e;
-      unsigned m;
-      if (MOEPERM_ROUTE_MATCH) {
-        m = __match_any_sync(0xffffffffu, e);
-      } else {
-        m = __ballot_sync(0xffffffffu, e >= 0);
-        for (int b = 0; b < nbits; ++b) {
-          const unsigned bit = (unsigned)(e >> b) & 1u;
-          const unsigned bal = __ballot_sync(0xffffffffu, bit);
-          m &= bit ? bal : ~bal;
-        }
-      }
+      const unsigned m = __match_any_sync(0xffffffffu, e);
       peers[j] = (e >= 0) ? m : 0u;
     }
 #pragma unroll

@@ -66,7 +66,7 @@ def _declare(L):
         "moe_dispatch_compact": (i32, [vp, i64, i32, vp, i32, vp, vp, i32, i32, i32, i32, i32, i32,
                                        vp, vp, i64, vp, i64, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]),
         "moe_dispatch_masked": (i32, [vp, i64, i32, vp, i32, vp, vp, i32, i32, i32, i32, i32, i32,
-                                      vp, vp, i64, vp, vp, vp, vp, sz, vp, vp]),
+                                      vp, vp, i64, vp, vp, vp, vp, i32, vp, sz, vp, vp]),
         "moe_dispatch_compact_noalloc": (i32, [vp, i64, i32, vp, i32, vp, vp, i32, i32, i32, i32,
                                                i32, i32, vp, vp, i64, vp, i64, vp, vp, vp, vp, vp,
                                                vp, vp, vp]),
@@ -171,12 +171,13 @@ def moe_dispatch_compact_noalloc(x, ldx, T, d_num_tokens, H, topk_ids, topk_weig
 
 
 def moe_dispatch_masked(x, ldx, T, d_num_tokens, H, topk_ids, topk_weights, K, E, L, cap, g,
-                        fmt, xq, scales, ld_s, masked_m, src2dst, row_weights, workspace,
-                        workspace_bytes, d_status, stream=None) -> int:
+                        fmt, xq, scales, ld_s, masked_m, src2dst, row_weights, psum, psum_align,
+                        workspace, workspace_bytes, d_status, stream=None) -> int:
     return int(lib().moe_dispatch_masked(
         _ptr(x), ldx, T, _ptr(d_num_tokens), H, _ptr(topk_ids), _ptr(topk_weights), K, E, L,
         cap, g, FMT[fmt], _ptr(xq), _ptr(scales), ld_s, _ptr(masked_m), _ptr(src2dst),
-        _ptr(row_weights), _ptr(workspace), workspace_bytes, _ptr(d_status), _stream(stream)))
+        _ptr(row_weights), _ptr(psum), psum_align, _ptr(workspace), workspace_bytes,
+        _ptr(d_status), _stream(stream)))
 
 
 def moe_quant_group(x, ldx, T_cap, d_num_live, H, g, fmt, xq, scales, ld_s, d_status,
@@ -300,8 +301,11 @@ def dispatch_compact(x, topk_ids, topk_weights, num_experts, num_local_experts, 
 
 def dispatch_masked(x, topk_ids, topk_weights, num_experts, num_local_experts, cap,
                     group_size=128, scale_fmt="packed", num_tokens=None, workspace=None,
-                    status=None, row_weights=True):
-    """Quantise + scatter into per-expert slabs [L, cap, H]. Returns a dict."""
+                    status=None, row_weights=True, psum_align=128):
+    """Quantise + scatter into per-expert slabs [L, cap, H]. Returns a dict,
+    including psum [L], the expanded layout of the slab rows aligned to
+    psum_align (None: not computed), and expand_rows, the static row count of
+    that layout."""
     T, H = x.shape
     K = topk_ids.shape[1]
     L = num_local_experts
@@ -313,13 +317,15 @@ def dispatch_masked(x, topk_ids, topk_weights, num_experts, num_local_experts, c
         masked_m=torch.empty(L, dtype=torch.int32, device=dev),
         src2dst=torch.empty((T, K), dtype=torch.int32, device=dev),
         row_weights=torch.empty(L * cap, dtype=torch.float32, device=dev) if row_weights else None,
+        psum=torch.empty(L, dtype=torch.int32, device=dev) if psum_align else None,
+        expand_rows=moe_compact_bound(T * K, L, psum_align) if psum_align else 0,
     )
     ws = workspace if workspace is not None else Workspace(T, K, L, dev)
     st = status if status is not None else torch.zeros(1, dtype=torch.int32, device=dev)
     code = moe_dispatch_masked(
         x, x.stride(0), T, num_tokens, H, topk_ids, topk_weights, K, num_experts, L, cap,
         group_size, scale_fmt, xq, sc, ld, out["masked_m"], out["src2dst"], out["row_weights"],
-        ws.buf, ws.nbytes, st)
+        out["psum"], psum_align or 1, ws.buf, ws.nbytes, st)
     _check(code, "moe_dispatch_masked")
     out["status"] = st
     return out

@@ -194,28 +194,35 @@ moe_status_t moe_dispatch_compact(
 
 /*
  * moe_dispatch_compact_noalloc -- moe_dispatch_compact without a caller-provided
- * workspace. The SGLang pages have no counterpart of this call.
+ * workspace. The SGLang pages have no counterpart of this call: it exists for
+ * callers of this library, not for the method.
  *
- * Who it is for: callers that cannot allocate device memory -- code running
- * while a CUDA graph is captured (allocation is not allowed there), plugins
- * whose host engine owns every allocation and passes in only inputs and
- * outputs, and serving loops that forbid allocation after start-up. It calls
- * no cudaMalloc, cudaFree or other allocating routine.
+ * Who it is for: callers that cannot allocate device memory -- a plugin whose
+ * host engine owns every device allocation and passes in only inputs and
+ * outputs, a serving loop that forbids allocation after start-up so that its
+ * memory footprint stays fixed, a runtime held to a fixed device-memory
+ * budget. It calls no cudaMalloc, cudaFree or other allocating routine.
  *
  * Arguments, outputs, results and errors are those of moe_dispatch_compact
- * without `workspace` / `workspace_bytes`. The scratch lives in one static
- * device array of 65,792 bytes (64 KiB + 256) that every GPU loading the
- * library holds until the process exits; a call whose moe_workspace_bytes(T,
- * K, L) exceeds it returns MOE_ERR_INVALID_ARG before any CUDA call (e.g. the
- * 8192-token, top-8, 256-expert prefill needs 16,640 bytes).
+ * without `workspace` / `workspace_bytes`; the caller still passes every input
+ * and output buffer. The scratch lives in one static device array of 65,792
+ * bytes (64 KiB + 256, the largest moe_workspace_bytes of any accepted size)
+ * that every GPU loading the library holds until the process exits; a call
+ * whose moe_workspace_bytes(T, K, L) is 0 or exceeds it returns
+ * MOE_ERR_INVALID_ARG before any CUDA work is enqueued.
  *
- * - The first call on each device looks up the array's device address
- *   (cudaGetSymbolAddress) with that device current; make that first call
- *   before any stream capture.
- * - Each call enqueues a memset that clears the part of the array it uses,
- *   then the two dispatch kernels, on `stream`.
- * - All calls share the one array: calls that can overlap on the GPU (other
- *   streams, other threads) race on it and must be serialised by the caller.
+ * - Set-up: the first call in each CUDA context (normally once per device)
+ *   looks up the array's device address with cudaGetSymbolAddress, with that
+ *   device current, and caches it under the context's id (a context created
+ *   again after cudaDeviceReset is looked up afresh). Make that first call on
+ *   each device before any stream capture begins.
+ * - Each call enqueues only the dispatch kernels on `stream`. Nothing in the
+ *   array needs to start at zero (every word a kernel reads was written
+ *   earlier in the same call), so a call clears nothing.
+ * - All calls share the one array and it keeps the last call's contents:
+ *   calls that can overlap on the GPU (calls on different streams, or from
+ *   different host threads) race on it and must be serialised by the caller,
+ *   e.g. by issuing them all on one stream.
  */
 moe_status_t moe_dispatch_compact_noalloc(
     const void* x, int64_t ldx, int32_t T, const int32_t* d_num_tokens, int32_t H,
@@ -232,12 +239,23 @@ moe_status_t moe_dispatch_compact_noalloc(
  *
  * Same inputs as moe_dispatch_compact, plus
  *   cap                          slab rows per local expert (max_m), >= 1
+ *   psum_align                   segment alignment of the psum output (>= 1;
+ *                                128 in [P3]); ignored when psum is NULL
  * Outputs
  *   xq [L, cap, H] e4m3          slab row (e, j) = j-th slot routed to e
  *   scales (fmt, ld_s)           for PACKED one block of `cap` rows per expert
  *   masked_m [L] int32           min(count, cap)
  *   src2dst [T, K] int32         e*cap + j, or -1 if dropped or past capacity
  *   row_weights [L*cap] f32      (optional)
+ *   psum [L] int32               (optional) the expanded (psum) layout of the
+ *                                slab's real rows [P3 实现拆解 item 3, 关键源码片段
+ *                                _build_layout]: psum[e] = align(psum[e-1],
+ *                                psum_align) + masked_m[e], psum[-1] = 0. It is
+ *                                the psum moe_expand_from_slab / moe_expand_to_slab
+ *                                take with align = psum_align, so a decode step
+ *                                can repack the slab without reading counts on
+ *                                the host; its rows fit moe_compact_bound(T*K, L,
+ *                                psum_align) expanded rows.
  * An expert with more than cap slots sets MOE_STATUS_OVERFLOW; its slots past
  * cap are not written (fail fast, never truncate silently: [P3 风险与影响 1]).
  * Workspace and launches as moe_dispatch_compact.
@@ -247,8 +265,8 @@ moe_status_t moe_dispatch_masked(
     const int32_t* topk_ids, const float* topk_weights, int32_t K, int32_t E, int32_t L,
     int32_t cap, int32_t g, moe_scale_fmt_t fmt,
     void* xq, void* scales, int64_t ld_s, int32_t* masked_m, int32_t* src2dst,
-    float* row_weights, void* workspace, size_t workspace_bytes, int32_t* d_status,
-    moe_stream_t stream);
+    float* row_weights, int32_t* psum, int32_t psum_align, void* workspace,
+    size_t workspace_bytes, int32_t* d_status, moe_stream_t stream);
 
 /*
  * moe_quant_group -- [P4 功能与动机 and 实现拆解 item 1: quantise on the send side

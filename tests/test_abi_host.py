@@ -95,13 +95,19 @@ def test_dispatch_compact_rejects(mp, over):
 def test_other_calls_reject(mp):
     S = _NullStream()
     E = mp.MOE_ERR_INVALID_ARG
-    # masked: bad cap, missing masked_m, packed ld below cap
+    # masked: bad cap, missing masked_m, packed ld below cap, psum with a zero alignment
     assert mp.moe_dispatch_masked(FAKE, 7168, 8, None, 7168, FAKE, FAKE, 8, 256, 32, 0, 128, "packed",
-                                  FAKE, FAKE, 4, FAKE, FAKE, None, FAKE, 1 << 20, FAKE, S) == E
+                                  FAKE, FAKE, 4, FAKE, FAKE, None, None, 128, FAKE, 1 << 20, FAKE,
+                                  S) == E
     assert mp.moe_dispatch_masked(FAKE, 7168, 8, None, 7168, FAKE, FAKE, 8, 256, 32, 16, 128, "packed",
-                                  FAKE, FAKE, 16, None, FAKE, None, FAKE, 1 << 20, FAKE, S) == E
+                                  FAKE, FAKE, 16, None, FAKE, None, None, 128, FAKE, 1 << 20, FAKE,
+                                  S) == E
     assert mp.moe_dispatch_masked(FAKE, 7168, 8, None, 7168, FAKE, FAKE, 8, 256, 32, 16, 128, "packed",
-                                  FAKE, FAKE, 12, FAKE, FAKE, None, FAKE, 1 << 20, FAKE, S) == E
+                                  FAKE, FAKE, 12, FAKE, FAKE, None, None, 128, FAKE, 1 << 20, FAKE,
+                                  S) == E
+    assert mp.moe_dispatch_masked(FAKE, 7168, 8, None, 7168, FAKE, FAKE, 8, 256, 32, 16, 128, "packed",
+                                  FAKE, FAKE, 16, FAKE, FAKE, None, FAKE, 0, FAKE, 1 << 20, FAKE,
+                                  S) == E
     # quant_group: packed with g = 32, odd pointer
     assert mp.moe_quant_group(FAKE, 7168, 112, None, 7168, 32, "packed", FAKE, FAKE, 112, FAKE, S) == E
     assert mp.moe_quant_group(ODD, 7168, 112, None, 7168, 32, "u8", FAKE, FAKE, 224, FAKE, S) == E

@@ -59,7 +59,8 @@ def compact_both(mp, ref, x, ids, w, H, K, E, L, b, g, fmt, n_live=None, ldx=Non
     return r, d, ws
 
 
-def masked_both(mp, ref, x, ids, w, H, K, E, L, cap, g, fmt, n_live=None):
+def masked_both(mp, ref, x, ids, w, H, K, E, L, cap, g, fmt, n_live=None, psum_align=128):
+    """Masked dispatch on both sides; psum_align None leaves the psum output out."""
     T = ids.shape[0]
     G = H // g
     r = {"xq": np.full((L * cap, H), 0xEE, np.uint8)}
@@ -67,16 +68,19 @@ def masked_both(mp, ref, x, ids, w, H, K, E, L, cap, g, fmt, n_live=None):
     r["mm"] = np.full(L, -5, np.int32)
     r["s2d"] = np.full((T, K), -9, np.int32)
     r["rw"] = np.full(L * cap, np.nan, np.float32)
+    if psum_align is not None:
+        r["psum"] = np.full(L, -5, np.int32)
     d = {k: to_dev(v.copy()) for k, v in r.items()}
     nl = T if n_live is None else n_live
     st_ref = ref.dispatch_masked(x, T, nl, H, ids, w, K, L, cap, g, fmt, r["xq"], r["sc"], ld,
-                                 r["mm"], r["s2d"], r["rw"])
+                                 r["mm"], r["s2d"], r["rw"], psum=r.get("psum"),
+                                 psum_align=psum_align or 1)
     ws = mp.Workspace(T, K, L, DEV)
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     nld = None if n_live is None else torch.tensor([n_live], dtype=torch.int32, device=DEV)
     code = mp.moe_dispatch_masked(bf16_dev(x), H, T, nld, H, to_dev(ids), to_dev(w), K, E, L, cap,
                                   g, fmt, d["xq"], d["sc"], ld, d["mm"], d["s2d"], d["rw"],
-                                  ws.buf, ws.nbytes, status)
+                                  d.get("psum"), psum_align or 1, ws.buf, ws.nbytes, status)
     assert code == mp.MOE_OK
     torch.cuda.synchronize()
     for k, v in r.items():
@@ -785,98 +789,6 @@ def test_graph_capture_scatter_above_48k_shared_memory(dev, ref):
         assert np.array_equal(out["xq"].cpu().numpy()[rows], rxq[rows])
         assert np.array_equal(out["scales"].cpu().numpy()[rows], rsc[rows])
     assert int(st.item()) == 0
-
-
-# ---------------------------------------------------------------------------
-# Full size, in the benchmark's launch configuration (prefill workload)
-# ---------------------------------------------------------------------------
-
-def full_size_sampled(dev, ref, x, ids, w, E, L, b=128, g=128):
-    """Compact dispatch + combine at full size, checked without running the
-    oracle over every byte. The layout does not depend on H, so the oracle run
-    on the first 128 columns gives the full layout and the first group of
-    every row bit-exactly; sampled tokens are checked over the whole row
-    (payload, every scale) and through the combine."""
-    T, H = x.shape
-    K = ids.shape[1]
-    out = dev.dispatch_compact(bf16_dev(x), to_dev(ids), to_dev(w), E, L, block_e=b, group_size=g,
-                               scale_fmt="packed")
-    torch.cuda.synchronize()
-    bound = out["bound"]
-    # oracle on the first group of columns (ldx = H, width 128)
-    rxq = np.zeros((bound, 128), np.uint8)
-    rsc, rld = ref.scale_buffer("packed", bound, 1, fill=0)
-    rmi = np.zeros(bound, np.int32)
-    rs2d = np.zeros((T, K), np.int32)
-    rc, rs, rp = (np.zeros(L, np.int32) for _ in range(3))
-    rt = np.zeros(1, np.int32)
-    rrw = np.full(bound, np.nan, np.float32)
-    ref.dispatch_compact(x, T, T, 128, ids, w, K, L, b, g, "packed", rxq, rsc, rld, rmi, bound, rs2d,
-                         rc, rs, rp, rt, rrw, ldx=H)
-    s2d = out["src2dst"].cpu().numpy()
-    assert np.array_equal(s2d, rs2d)
-    assert np.array_equal(out["m_indices"].cpu().numpy(), rmi)
-    assert np.array_equal(out["counts"].cpu().numpy(), rc)
-    assert np.array_equal(out["starts"].cpu().numpy(), rs)
-    assert np.array_equal(out["psum"].cpu().numpy(), rp)
-    assert int(out["total"].item()) == int(rt[0])
-    rows = s2d[s2d >= 0]
-    xq = out["xq"]
-    got_g0 = xq[torch.from_numpy(rows).to(DEV).long(), :128].cpu().numpy()
-    assert np.array_equal(got_g0, rxq[rows])
-    rw = out["row_weights"].cpu().numpy()
-    assert np.array_equal(rw[rows], rrw[rows])
-    sc_words = out["scales"].cpu().numpy().reshape(-1, out["ld_s"])       # [G4, ld] int32
-    g0 = (sc_words[0, rows] & 0xFF).astype(np.uint8)
-    want_g0 = rsc.view(np.int32).reshape(-1, rld)[0, rows].astype(np.uint32) & 0xFF
-    assert np.array_equal(g0, want_g0.astype(np.uint8))
-    # sampled tokens: whole rows and all scales
-    rng = np.random.default_rng(0)
-    for t in rng.choice(T, size=24, replace=False):
-        q, eb = ref.quant_row(x[t], g)
-        for k in range(K):
-            row = s2d[t, k]
-            assert row >= 0
-            assert np.array_equal(xq[row].cpu().numpy(), q)
-            words = sc_words[:, row].astype(np.uint32)
-            got_eb = np.stack([(words >> (8 * i)) & 0xFF for i in range(4)], axis=1).reshape(-1)[:H // g]
-            assert np.array_equal(got_eb.astype(np.uint8), eb)
-    # combine of sampled tokens against the fp32-FMA twin
-    gen = torch.Generator(device=DEV)
-    gen.manual_seed(11)
-    y = torch.randn((bound, H), generator=gen, device=DEV).to(torch.bfloat16)
-    o = dev.combine(y, out["src2dst"], to_dev(w))
-    torch.cuda.synchronize()
-    sample = rng.choice(T, size=32, replace=False)
-    for t in sample:
-        yr = y[torch.from_numpy(s2d[t]).to(DEV).long()].view(torch.int16).cpu().numpy().view(np.uint16)
-        want = ref.combine_f32(np.ascontiguousarray(yr), np.arange(K, dtype=np.int32)[None, :],
-                               np.ascontiguousarray(w[t:t + 1]), 1, K, H)
-        got = o[t].view(torch.int16).cpu().numpy().view(np.uint16)
-        assert np.array_equal(got, want[0])
-
-
-
-
-def test_prefill_full_size_sampled(dev, ref):
-    """T = 8192, H = 7168, 256 local experts, top-8 Zipf routing, block_e 128,
-    packed UE8M0: the call bench.py times."""
-    d = synth.prefill(0)
-    c = d["cfg"]
-    assert (c["block_e"], c["g"]) == (128, 128)
-    full_size_sampled(dev, ref, d["x"], d["topk_ids"], d["topk_weights"], c["E"], c["L"])
-
-
-@pytest.mark.parametrize("T,H,E,K", [(16384, 2048, 64, 6), (8192, 5120, 160, 6)])
-def test_sweep_shapes_full_size_sampled(dev, ref, T, H, E, K):
-    """Two shapes of the shape sweep at full size: narrow rows (one chunk per
-    scatter thread, the small route-plan table) and top-6 over 160 experts
-    (3 + 3 row batches in the combine)."""
-    rng = np.random.default_rng(T + H + E + K)
-    x = synth.normal_bf16(rng, (T, H))
-    ids = synth.zipf_topk(rng, T, E, K, n_empty=12)
-    w = synth.softmax_weights(rng, T, K)
-    full_size_sampled(dev, ref, x, ids, w, E, E)
 
 
 # ---------------------------------------------------------------------------

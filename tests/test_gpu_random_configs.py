@@ -62,7 +62,8 @@ def test_random_masked_dispatch(dev, ref, seed):
     n_live = None if rng.random() < 0.5 else int(rng.integers(0, T + 1))
     x = synth.normal_bf16(rng, (T, H), outlier_frac=0.01)
     w = synth.softmax_weights(rng, T, K)
-    masked_both(dev, ref, x, ids, w, H, K, E, L, cap, g, fmt, n_live=n_live)
+    psum_align = [None, 1, 8, 128][int(rng.integers(0, 4))]   # None: no psum output
+    masked_both(dev, ref, x, ids, w, H, K, E, L, cap, g, fmt, n_live=n_live, psum_align=psum_align)
 
 
 @pytest.mark.parametrize("seed", range(10))
