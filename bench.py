@@ -934,6 +934,40 @@ def shape_sweep(args):
         del graphs, y, xq, x
 
 
+def only_dispatch(args):
+    """The prefill dispatch call alone (route plan + quantise/scatter), W
+    warm-up calls then K calls through the C ABI, with no expert outputs
+    allocated (about 0.8 GB on the device): the case profiler captures of the
+    dispatch kernels run on. Prints one JSON line."""
+    import torch
+
+    import combine_fp8_quant_gb300 as mp
+    from combine_fp8_quant_gb300 import build as cuda_build
+    cuda_build.build()
+    mp.load()
+    dev = torch.device("cuda:0")
+    d = synth.prefill(0, T=args.tokens)
+    c = d["cfg"]
+    T, H, K, E, L, b, g = c["T"], c["H"], c["K"], c["E"], c["L"], c["block_e"], c["g"]
+    x = torch.from_numpy(d["x"].view(np.int16)).to(dev).view(torch.bfloat16)
+    ids = torch.from_numpy(d["topk_ids"]).to(dev)
+    bound = mp.moe_compact_bound(T * K, L, b)
+    ws = mp.Workspace(T, K, L, dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    xq = torch.empty((bound, H), dtype=torch.uint8, device=dev)
+    sc, ld = mp.scale_tensor("packed", bound, H, g, dev)
+    mi = torch.empty(bound, dtype=torch.int32, device=dev)
+    s2d = torch.empty((T, K), dtype=torch.int32, device=dev)
+    c3 = [torch.empty(L, dtype=torch.int32, device=dev) for _ in range(3)]
+    tot = torch.empty(1, dtype=torch.int32, device=dev)
+    for _ in range(args.warmup + args.steps):
+        assert mp.moe_dispatch_compact(x, H, T, None, H, ids, None, K, E, L, b, g, "packed", xq, sc, ld,
+                                       mi, bound, s2d, *c3, tot, None, ws.buf, ws.nbytes, st) == 0
+    torch.cuda.synchronize()
+    assert mp.moe_status_sync(st) == 0
+    print(json.dumps({"only_dispatch": True, "T": T, "calls": args.warmup + args.steps}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -943,6 +977,9 @@ def main():
     ap.add_argument("--only-step", action="store_true",
                     help="time the dispatch + combine step only (no e2e, other rows or CPU "
                          "baseline); used for profiler captures")
+    ap.add_argument("--only-dispatch", action="store_true",
+                    help="run W + K prefill dispatch calls and nothing else; for profiler "
+                         "captures of the dispatch kernels")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override T of the prefill workload (profiling smaller cases)")
     ap.add_argument("--layout-sweep", action="store_true",
@@ -950,6 +987,9 @@ def main():
     ap.add_argument("--shape-sweep", action="store_true",
                     help="the dispatch + combine step on other (T, H, E, K) shapes; one JSON line per shape")
     args = ap.parse_args()
+    if args.only_dispatch:
+        only_dispatch(args)
+        return
     if args.layout_sweep:
         layout_sweep(args)
         return

@@ -242,13 +242,15 @@ __device__ __forceinline__ int64_t align_up64(int64_t c, int64_t b) { return (c 
 // Segment starts of a layout whose segments are padded to multiples of b, in
 // expert order: st[e] = sum over e' < e of align(min(cnt[e'], clamp), b), for
 // e < L (PR #33128 compact starts; PR #29525 _build_layout starts). One CTA:
-// thread i owns a contiguous run of experts, a warp scan and a scan over the
-// warp totals join the runs. Returns the total in every thread. Every thread
-// of the CTA must call it (blockDim.x a multiple of 32); it begins reading cnt
-// and ends with a barrier. s_wsum: at least blockDim.x / 32 ints of shared memory.
+// thread i owns a contiguous run of experts; a warp scan joins the runs of a
+// warp and warp 0 scans the warp totals. Returns the total in every thread.
+// Every thread of the CTA must call it (blockDim.x a multiple of 32); it
+// begins reading cnt and ends with a barrier. s_wsum: at least 33 ints of
+// shared memory.
 __device__ __forceinline__ int aligned_starts(const int32_t* cnt, int32_t* st, int L, int b,
                                               int clamp, int32_t* s_wsum) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, bd = blockDim.x;
+  const int nwarps = bd >> 5;
   const int per = (L + bd - 1) / bd;
   const int lo = min(tid * per, L), hi = min(lo + per, L);
   int local = 0;
@@ -261,16 +263,25 @@ __device__ __forceinline__ int aligned_starts(const int32_t* cnt, int32_t* st, i
   }
   if (lane == 31) s_wsum[warp] = incl;
   __syncthreads();
-  int wbase = 0, total = 0;
-  for (int w = 0; w < (bd >> 5); ++w) {
-    if (w < warp) wbase += s_wsum[w];
-    total += s_wsum[w];
+  if (warp == 0) {  // exclusive scan of the warp totals; the grand total in s_wsum[32]
+    const int v = lane < nwarps ? s_wsum[lane] : 0;
+    int x = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int nb = __shfl_up_sync(0xffffffffu, x, off);
+      if (lane >= off) x += nb;
+    }
+    __syncwarp();
+    if (lane < nwarps) s_wsum[lane] = x - v;
+    if (lane == 31) s_wsum[32] = x;
   }
-  int run = wbase + incl - local;
+  __syncthreads();
+  int run = s_wsum[warp] + incl - local;
   for (int e = lo; e < hi; ++e) {
     st[e] = run;
     run += (min(cnt[e], clamp) + b - 1) / b * b;
   }
+  const int total = s_wsum[32];
   __syncthreads();
   return total;
 }

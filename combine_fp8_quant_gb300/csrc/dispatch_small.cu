@@ -41,7 +41,7 @@ constexpr int kCPT = 2;
 template <int GSZ, int FMT, int S>
 __global__ void __launch_bounds__(kThreads) dispatch_small_kernel(ScatterArgs p) {
   extern __shared__ int32_t sm[];
-  __shared__ int32_t s_wsum[kWarps];
+  __shared__ int32_t s_wsum[33];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int L = p.L, K = p.K, H = p.H;
   const int nch = H / 16, G = H / GSZ, G4 = (G + 3) / 4;

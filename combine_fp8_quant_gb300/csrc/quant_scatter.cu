@@ -253,7 +253,7 @@ __device__ __forceinline__ int slot_row(const ScatterArgs& p, const int32_t* tbl
 template <int GSZ, int FMT, int CPT>
 __global__ void __launch_bounds__(1024, 1) quant_scatter_kernel(ScatterArgs p) {
   extern __shared__ int32_t sm[];
-  __shared__ int32_t s_wsum[32];
+  __shared__ int32_t s_wsum[33];
   __shared__ int32_t s_nlist;
   const int tid = threadIdx.x, lane = tid & 31, bd = blockDim.x;
   const int H = p.H;
