@@ -25,8 +25,10 @@
  *   - Every data call enqueues its kernels on `stream` and returns without
  *     waiting. The grid of every launch depends only on scalar arguments and
  *     the device's SM count, never on routing contents or device-side counts,
- *     so every call can be captured in a CUDA graph and replayed with new
- *     contents of the same shapes.
+ *     so every call that takes its buffers from the caller (all but
+ *     moe_dispatch_compact_noalloc, described on its own below) can be
+ *     captured in a CUDA graph and replayed with new contents of the same
+ *     shapes.
  *   - Argument errors (null required pointer, misalignment, unsupported
  *     sizes / format / group pairs, a workspace that is too small) return
  *     MOE_ERR_INVALID_ARG before anything is launched.
