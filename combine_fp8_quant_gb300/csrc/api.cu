@@ -1,6 +1,7 @@
 // api.cu -- the C ABI of libmoeperm (include/moeperm.h): host-side argument
 // validation, workspace carving and kernel launches. No allocation, no
 // synchronisation (except moe_status_sync), no host <-> device traffic.
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -10,23 +11,62 @@
 #include "common.cuh"
 #include "kernels.h"
 
-// Host-side caches of launch queries, per device. An occupancy query or a
-// device attribute read costs the host about as much as a launch, and a
-// shared-memory opt-in more; each is asked once per key. The tables are
-// small and fixed: once one is full, new keys are simply asked every time.
+// Host-side caches of launch queries. An occupancy query or a device
+// attribute read costs the host about as much as a launch, and a
+// shared-memory opt-in more; each is asked once per key. Occupancy and device
+// attributes are properties of the device; the shared-memory opt-in is a
+// function attribute of the CUDA context, so it is cached per context (a
+// context created again after cudaDeviceReset has a new id and opts in
+// afresh). The tables are small and fixed: once one is full, new keys are
+// simply asked every time.
 namespace moeperm {
 namespace {
 std::mutex g_cache_mu;
 struct OccEntry { const void* kernel; int threads; size_t smem; int dev; int value; };
 OccEntry g_occ[256];
 int g_nocc = 0;
-struct SmemEntry { const void* kernel; int dev; size_t dyn; };
+struct SmemEntry { const void* kernel; unsigned long long ctx; size_t dyn; };
 SmemEntry g_smem[128];
 int g_nsmem = 0;
 struct AttrEntry { int attr; int dev; int value; };
 AttrEntry g_attr[64];
 int g_nattr = 0;
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+std::once_flag g_ctx_once;
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
+
+// Driver entry points for the current context and its id, looked up once
+// through the runtime (the library does not link the driver library).
+void find_context_entry_points() {
+  void* f1 = nullptr;
+  void* f2 = nullptr;
+  cudaDriverEntryPointQueryResult q1 = cudaDriverEntryPointSymbolNotFound;
+  cudaDriverEntryPointQueryResult q2 = cudaDriverEntryPointSymbolNotFound;
+  if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 12000, cudaEnableDefault, &q1) !=
+          cudaSuccess ||
+      cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2) !=
+          cudaSuccess ||
+      q1 != cudaDriverEntryPointSuccess || q2 != cudaDriverEntryPointSuccess) {
+    (void)cudaGetLastError();
+    return;
+  }
+  g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(f1);
+  g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(f2);
+}
 }  // namespace
+
+cudaError_t current_context_id(unsigned long long* id) {
+  *id = 0;
+  std::call_once(g_ctx_once, find_context_entry_points);
+  if (g_ctx_get_current == nullptr || g_ctx_get_id == nullptr) return cudaErrorSymbolNotFound;
+  CUcontext ctx = nullptr;
+  if (g_ctx_get_current(&ctx) != CUDA_SUCCESS) return cudaErrorUnknown;
+  if (ctx == nullptr) return cudaSuccess;
+  return g_ctx_get_id(ctx, id) == CUDA_SUCCESS ? cudaSuccess : cudaErrorUnknown;
+}
 
 cudaError_t occupancy_cached(const void* kernel, int threads, size_t smem, int* per_sm) {
   int dev = 0;
@@ -50,23 +90,27 @@ cudaError_t occupancy_cached(const void* kernel, int threads, size_t smem, int* 
 }
 
 cudaError_t opt_in_smem_cached(const void* kernel, size_t dyn) {
-  int dev = 0;
-  cudaError_t err = cudaGetDevice(&dev);
-  if (err != cudaSuccess) return err;
-  {
+  unsigned long long ctx = 0;
+  // no context id (none current yet, or no driver entry point): set the
+  // attribute every time rather than trust a cache entry
+  const bool cacheable = current_context_id(&ctx) == cudaSuccess && ctx != 0;
+  if (cacheable) {
     std::lock_guard<std::mutex> g(g_cache_mu);
     for (int i = 0; i < g_nsmem; ++i)
-      if (g_smem[i].kernel == kernel && g_smem[i].dev == dev && g_smem[i].dyn >= dyn) return cudaSuccess;
+      if (g_smem[i].kernel == kernel && g_smem[i].ctx == ctx && g_smem[i].dyn >= dyn) return cudaSuccess;
   }
-  err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+  cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
   if (err != cudaSuccess) return err;
+  if (!cacheable) return cudaSuccess;
+  err = current_context_id(&ctx);  // the call above may have created the context
+  if (err != cudaSuccess || ctx == 0) return cudaSuccess;
   std::lock_guard<std::mutex> g(g_cache_mu);
   for (int i = 0; i < g_nsmem; ++i)
-    if (g_smem[i].kernel == kernel && g_smem[i].dev == dev) {
+    if (g_smem[i].kernel == kernel && g_smem[i].ctx == ctx) {
       if (g_smem[i].dyn < dyn) g_smem[i].dyn = dyn;
       return cudaSuccess;
     }
-  if (g_nsmem < 128) g_smem[g_nsmem++] = SmemEntry{kernel, dev, dyn};
+  if (g_nsmem < 128) g_smem[g_nsmem++] = SmemEntry{kernel, ctx, dyn};
   return cudaSuccess;
 }
 

@@ -225,6 +225,8 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 // memory. Without the opt-in a CTA is limited to 48 KiB of dynamic plus static
 // shared memory; the static arrays of these kernels stay under 1 KiB.
 cudaError_t occupancy_cached(const void* kernel, int threads, size_t smem, int* per_sm);
+// Unique id of the CUDA context current on this thread (0 when none is).
+cudaError_t current_context_id(unsigned long long* id);
 cudaError_t opt_in_smem_cached(const void* kernel, size_t dyn);
 cudaError_t device_attr_cached(cudaDeviceAttr attr, int* value);
 template <typename Kern>

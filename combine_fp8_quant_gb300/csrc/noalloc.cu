@@ -25,13 +25,13 @@
 // chunk-table word before the scatter reads it and resets the token counter
 // itself, so a call neither clears the array nor depends on what the previous
 // call left in it.
-#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 #include <mutex>
 
 #include "../../include/moeperm.h"
+#include "common.cuh"
 
 namespace {
 
@@ -39,9 +39,6 @@ namespace {
 // plus the 256-byte reserved header.
 constexpr size_t kNoAllocScratchBytes = 64 * 1024 + 256;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
-
-using CtxGetCurrentFn = CUresult (*)(CUcontext*);
-using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
 
 struct ScratchEntry {
   unsigned long long ctx_id;
@@ -52,47 +49,15 @@ std::mutex g_setup_mutex;
 ScratchEntry g_entries[kMaxEntries];
 int g_nentries = 0;
 int g_next = 0;  // entry replaced when the table is full
-CtxGetCurrentFn g_ctx_get_current = nullptr;
-CtxGetIdFn g_ctx_get_id = nullptr;
-
-// Driver entry points for the current context and its id, looked up through
-// the runtime (the library does not link the driver library directly).
-cudaError_t driver_entry_points() {
-  if (g_ctx_get_current != nullptr && g_ctx_get_id != nullptr) return cudaSuccess;
-  void* f1 = nullptr;
-  void* f2 = nullptr;
-  cudaDriverEntryPointQueryResult q1 = cudaDriverEntryPointSymbolNotFound;
-  cudaDriverEntryPointQueryResult q2 = cudaDriverEntryPointSymbolNotFound;
-  cudaError_t err = cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 12000,
-                                                     cudaEnableDefault, &q1);
-  if (err != cudaSuccess) return err;
-  err = cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2);
-  if (err != cudaSuccess) return err;
-  if (q1 != cudaDriverEntryPointSuccess || q2 != cudaDriverEntryPointSuccess || !f1 || !f2)
-    return cudaErrorSymbolNotFound;
-  g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(f1);
-  g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(f2);
-  return cudaSuccess;
-}
-
-// Unique id of the context current on this thread (0 when none is).
-cudaError_t current_context_id(unsigned long long* id) {
-  *id = 0;
-  CUcontext ctx = nullptr;
-  if (g_ctx_get_current(&ctx) != CUDA_SUCCESS) return cudaErrorUnknown;
-  if (ctx == nullptr) return cudaSuccess;
-  return g_ctx_get_id(ctx, id) == CUDA_SUCCESS ? cudaSuccess : cudaErrorUnknown;
-}
 
 // Device address of the scratch array in the current context; the first call
 // in a context looks it up (which also initialises the device's primary
 // context if no context is current yet).
 cudaError_t scratch_address(void** out) {
+  using moeperm::current_context_id;
   std::lock_guard<std::mutex> lock(g_setup_mutex);
-  cudaError_t err = driver_entry_points();
-  if (err != cudaSuccess) return err;
   unsigned long long id = 0;
-  err = current_context_id(&id);
+  cudaError_t err = current_context_id(&id);
   if (err != cudaSuccess) return err;
   if (id != 0)
     for (int i = 0; i < g_nentries; ++i)
