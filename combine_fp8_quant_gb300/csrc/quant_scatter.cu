@@ -33,7 +33,8 @@
 //   (programmatic dependent launch), so before waiting for it a CTA reads and
 //   quantises its first few tokens into their staging buffers (inputs only:
 //   their rows are not known yet) and loads the expert ids of its first slots
-//   (one per thread). After the wait it loads the chunk table (<= 64 KiB)
+//   (one per thread). After the wait it bulk-prefetches the rows of its next
+//   few tokens into L2 and loads the chunk table (<= 64 KiB)
 //   into shared memory, scans it, and resolves the rows of all of its own
 //   slots at once. The route plan therefore needs no serial "last block" and
 //   no fence. Tokens with no kept slot (all their experts remote) are dropped
@@ -74,9 +75,12 @@ constexpr int kPre = 2;
 constexpr int kCpt1MaxH = 5120;
 static_assert(kCpt1MaxH <= 16384, "one chunk per thread covers at most 1024 x 16 elements");
 // Tokens after the early-staged ones whose x rows are bulk-prefetched into L2
-// (evict_last) before the wait on the route plan, while HBM is mostly idle
-// (staged path; whole step 266.8 -> 265.6 us with 2).
-constexpr int kPrefetchEarly = 2;
+// (evict_last) right after the wait on the route plan, so that the reads run
+// while the CTA builds the layout instead of delaying the wait (staged path;
+// measured against 2 tokens before the wait: dispatch 105.1-105.8 -> 104.0-104.4 us,
+// step 266.9-267.7 -> 265.6-266.1 us; 2 / 4 / 8 / 10 / 14 after the wait:
+// 104.7 / 104.6 / 105.1 / 104.8 / 108.1 us).
+constexpr int kPrefetchAfterWait = 6;
 // Direct stores instead of staging when the expected kept slots per token,
 // K * L / E (uniform routing), are at most this many (staged -> direct at
 // T = 8192, H = 7168: f = 1 47.1 -> 43.0 us, f = 3 62.9 -> 61.5, f = 4
@@ -293,11 +297,6 @@ __global__ void __launch_bounds__(1024, 1) quant_scatter_kernel(ScatterArgs p) {
     // route plan still runs (their rows are not known yet); their scales wait
     // in shared memory.
     npre = p.direct ? 0 : (ntok < p.pre ? ntok : p.pre);
-    if (kPrefetchEarly > 0 && !p.direct && tid == 0) {
-      const uint64_t pol = l2_policy_evict_last();
-      for (int j = npre; j < ntok && j < npre + kPrefetchEarly; ++j)
-        bulk_prefetch_l2_hint(p.x + (int64_t)(blockIdx.x + j * gridDim.x) * p.ldx, (uint32_t)(2 * H), pol);
-    }
     for (int j = 0; j < npre; ++j) {
       uint4 vn[CPT][2];
       load_row(vn, j + 1 < npre ? p.x + (int64_t)(blockIdx.x + (j + 1) * gridDim.x) * p.ldx : nullptr,
@@ -320,6 +319,11 @@ __global__ void __launch_bounds__(1024, 1) quant_scatter_kernel(ScatterArgs p) {
     }
 
     pdl_wait_primary();
+    if (!p.direct && tid == 0) {  // the rows of the next tokens into L2 while the layout is built
+      const uint64_t pol = l2_policy_evict_last();
+      for (int j = npre; j < ntok && j < npre + kPrefetchAfterWait; ++j)
+        bulk_prefetch_l2_hint(p.x + (int64_t)(blockIdx.x + j * gridDim.x) * p.ldx, (uint32_t)(2 * H), pol);
+    }
     const int lr0 = a0 >= 0 ? __ldcg(p.src2dst + a0) : -1;  // in flight with the table loads
     const int L = p.L;
     int32_t* tbl = sm;
