@@ -86,6 +86,8 @@ struct ScatterArgs {
   int32_t direct;              // scatter: 1 = direct stores, no staging (few kept slots per token)
   int32_t* queue;              // direct mode: token counter, reset to 0 by the route plan
   int32_t dyn;                 // direct mode: tokens taken from the counter (set at launch)
+  int32_t nstat;               // staged mode: static tokens per CTA, the rest from the counter
+                               // (0: every token static; set at launch)
 };
 cudaError_t launch_quant_scatter(const ScatterArgs& a, int g, int fmt, int num_sms,
                                  bool after_route_plan, cudaStream_t s);

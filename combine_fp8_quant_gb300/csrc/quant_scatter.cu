@@ -25,7 +25,11 @@
 //   fixed strided set, so that CTAs end together (see the loop below).
 //
 // Design: a persistent grid (SMs x resident CTAs, independent of the routing)
-// walks the live tokens, t = blockIdx.x + i * gridDim.x. One thread owns two
+// walks the live tokens, t = blockIdx.x + i * gridDim.x -- in the staged mode
+// with enough tokens per CTA only the first part of them, the rest coming from
+// a token counter once a CTA's own tokens are done (SMs differ in how fast
+// they drain their stores, so a fixed split leaves the slowest SMs working
+// alone at the end; the tail loop below). One thread owns two
 // 16-element chunks of a row (two 16-byte loads each), so a single pass
 // covers H <= 32768; rows up to 5120 elements take one chunk per thread
 // instead, so that their CTAs keep enough threads (and loads) in flight.
@@ -81,6 +85,19 @@ static_assert(kCpt1MaxH <= 16384, "one chunk per thread covers at most 1024 x 16
 // step 266.9-267.7 -> 265.6-266.1 us; 2 / 4 / 8 / 10 / 14 after the wait:
 // 104.7 / 104.6 / 105.1 / 104.8 / 108.1 us).
 constexpr int kPrefetchAfterWait = 6;
+// Staged mode, tail from the token counter: with at least kTailMinTokens
+// tokens per CTA, a CTA's last tokens' worth are not assigned statically but
+// taken from a counter once its static tokens are done, so that CTAs on
+// faster SMs take more of them (per-CTA loop ends on the prefill spread from
+// 83 to 99 us, SM by SM). Wide rows (two chunks per thread) leave
+// ceil(kTailPct% of T / grid) tokens per CTA to the tail, narrow rows one.
+// Dispatch us, tail 0 / 1 / 3 / 8 / 9 / 32 tokens per CTA: T = 8192, H = 7168
+// (17 per CTA) 103.8 / 103.2 / 102.3 / 101.1-101.3 / 100.9 / -; T = 32768
+// (71 per CTA) 391.5 / 389.0 / 383.6 / 381.0 / 380.7 / 373.2; T = 4096
+// (8 per CTA) 57.8 / 58.2 / 62.0; narrow rows, tail 0 / 1 / 3: H = 4096
+// 66.3 / 62.4 / 64.0, H = 5120 64.9 / 64.5 / 65.6, H = 2048 55.6 / 53.8 / 55.7.
+constexpr int kTailMinTokens = 12;
+constexpr int kTailPct = 45;
 // Direct stores instead of staging when the expected kept slots per token,
 // K * L / E (uniform routing), are at most this many (staged -> direct at
 // T = 8192, H = 7168: f = 1 47.1 -> 43.0 us, f = 3 62.9 -> 61.5, f = 4
@@ -143,7 +160,7 @@ __device__ __forceinline__ void load_row(uint4 (&v)[CPT][2], const uint16_t* xro
 // base (st: compact start, masked 0) and, for compact, psum (ps).
 __device__ void layout_prologue(const ScatterArgs& p, int32_t* tbl, int32_t* st, int32_t* ps,
                                 int32_t* s_wsum) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, bd = blockDim.x;
+  const int tid = threadIdx.x, bd = blockDim.x;
   const int L = p.L, NC = p.nchunks;
   // the whole table in flight at once: 16-byte asynchronous copies (the
   // table starts 16-byte aligned in the workspace), the odd tail by loads
@@ -259,6 +276,12 @@ __global__ void __launch_bounds__(1024, 1) quant_scatter_kernel(ScatterArgs p) {
   extern __shared__ int32_t sm[];
   __shared__ int32_t s_wsum[33];
   __shared__ int32_t s_nlist;
+  // tokens taken from the counter (direct mode with the counter, or the
+  // staged mode's tail; never both in one launch): a ring of entries, each a
+  // token and the rows and experts of its slots (K <= 32)
+  __shared__ int32_t s_q[3];
+  __shared__ int32_t s_qrows[3][32];
+  __shared__ int32_t s_qexps[3][32];
   const int tid = threadIdx.x, lane = tid & 31, bd = blockDim.x;
   const int H = p.H;
   const int nch = H / 16;
@@ -268,8 +291,10 @@ __global__ void __launch_bounds__(1024, 1) quant_scatter_kernel(ScatterArgs p) {
   const int nslots = identity ? 1 : p.K;
   const int n_live = live_count(p.d_num_tokens, p.T, p.status,
                                 identity && blockIdx.x == 0 && tid == 0);
-  const int ntok =
+  const int ntok_all =
       n_live > (int)blockIdx.x ? (n_live - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  const bool tail = p.nstat > 0;  // staged mode only (set at launch)
+  const int ntok = tail && ntok_all > p.nstat ? p.nstat : ntok_all;  // static tokens of this CTA
   const bool dyn = p.dyn != 0;  // direct mode with the token counter (one extra warp, see below)
   const int nsl = identity || dyn ? 0 : ntok * p.K;  // slots of this CTA: i -> token i / K, slot i % K
   auto slot_of = [&](int i) -> int64_t {
@@ -421,9 +446,6 @@ __global__ void __launch_bounds__(1024, 1) quant_scatter_kernel(ScatterArgs p) {
   // other warps quantise and store the current one and load the next one; a
   // barrier per token publishes the producer's slot.
   if (dyn) {
-    __shared__ int32_t s_q[3];
-    __shared__ int32_t s_qrows[3][32];
-    __shared__ int32_t s_qexps[3][32];
     const int bdc = bd - 32;
     const bool producer = tid >= bdc;
     const int K = p.K;
@@ -546,7 +568,8 @@ __global__ void __launch_bounds__(1024, 1) quant_scatter_kernel(ScatterArgs p) {
   // evict_first on the payload rows: nothing here reads them back (prefill
   // 103.1-103.4 -> 103.1-103.3 us, 32 of 256 experts local 47.1 -> 45.1 us)
   const uint64_t st_policy = l2_policy_evict_first();
-  for (int n = 0; n < nlist; ++n) {
+  int n = 0;
+  for (; n < nlist; ++n) {
     const int it = identity ? n : list_s[n];
     const int t = blockIdx.x + it * gridDim.x;
     const bool staged = n < npre;  // the staged tokens are list entries 0 .. npre-1
@@ -602,6 +625,84 @@ __global__ void __launch_bounds__(1024, 1) quant_scatter_kernel(ScatterArgs p) {
         v[i][0] = vn[i][0];
         v[i][1] = vn[i][1];
       }
+    }
+  }
+
+  // ---- tail: tokens [nstat * grid, n_live) from the counter the route plan
+  // reset, each taken exactly once. Warp 0 claims the next token with a kept
+  // slot and resolves its rows (rewriting its src2dst entries) into the other
+  // of two ring entries while the current token is quantised; the staging
+  // ring and its barrier continue from the static loop. Claiming only one
+  // token ahead keeps the counter's tokens free for the CTAs that finish
+  // first (claiming two ahead, with the next row loaded one token ahead as in
+  // the static loop, measured 106.1-106.6 against 103.6-104.1 us).
+  if (tail) {
+    const int K = p.K;
+    const int64_t pool0 = (int64_t)p.nstat * gridDim.x;
+    int32_t* s_dt = s_q;
+    auto claim = [&](int slot) {  // warp 0 only
+      for (;;) {
+        int tc = 0;
+        if (lane == 0) tc = (int)(pool0 + atomicAdd(p.queue, 1));
+        tc = __shfl_sync(0xffffffffu, tc, 0);
+        if (tc >= n_live) {
+          if (lane == 0) s_dt[slot] = n_live;
+          return;
+        }
+        if (lane == 0)
+          bulk_prefetch_l2_hint(p.x + (int64_t)tc * p.ldx, (uint32_t)(2 * H), l2_policy_evict_last());
+        bool kept = false;
+        for (int k = lane; k < K; k += 32) {
+          const int64_t a = (int64_t)tc * K + k;
+          const int e = __ldg(p.ids + a);
+          const int row = slot_row(p, sm, st, a, e, __ldcg(p.src2dst + a));
+          p.src2dst[a] = row;
+          if (row >= 0 && p.row_weights != nullptr) p.row_weights[row] = __ldg(p.w + a);
+          s_qrows[slot][k] = row;
+          s_qexps[slot][k] = e;
+          kept |= row >= 0;
+        }
+        if (__any_sync(0xffffffffu, kept)) {
+          if (lane == 0) s_dt[slot] = tc;
+          return;
+        }
+      }
+    };
+    if (tid < 32) claim(0);
+    __syncthreads();
+    int t = s_dt[0];
+    load_row(v, t < n_live ? p.x + (int64_t)t * p.ldx : nullptr, nch, bd, tid);
+    for (int k = 0; t < n_live; ++k, ++n) {
+      const int cur = k & 1;
+      if (tid < 32) claim(cur ^ 1);  // the next token, while this one's row arrives
+      const int* rows = s_qrows[cur];
+      const int* exps = s_qexps[cur];
+      const int buf = n % p.stages;
+      uint8_t* sb = stage + (size_t)buf * H;
+#pragma unroll
+      for (int i = 0; i < CPT; ++i) {
+        const int c = i * bd + tid;
+        const bool active = c < nch;
+        int e;
+        float sval;
+        const uint4 qv = quant_chunk<GSZ, FMT>(v[i][0], v[i][1], e, sval);
+        if (active) *reinterpret_cast<uint4*>(sb + c * 16) = qv;
+        const int cw = i * bd + (tid & ~31);
+        if (cw < nch) store_scales<GSZ, FMT>(p, K, rows, exps, lane, active, e, sval, cw * 16 / GSZ, G, G4);
+      }
+      fence_proxy_async_smem();
+      if (tid == 0) wait_ring(p.stages);
+      __syncthreads();
+      if (tid == 0) {
+        for (int j = 0; j < K; ++j) {
+          const int row = rows[j];
+          if (row < 0) continue;
+          bulk_store_s2g_hint(p.xq + (int64_t)row * H, stage_s + (uint32_t)(buf * H), (uint32_t)H, st_policy);
+        }
+        bulk_commit();
+      }
+      t = s_dt[cur ^ 1];
+      load_row(v, t < n_live ? p.x + (int64_t)t * p.ldx : nullptr, nch, bd, tid);
     }
   }
 
@@ -666,6 +767,12 @@ cudaError_t launch_one(const ScatterArgs& a0, int num_sms, bool pdl, cudaStream_
   if (grid < 1) grid = 1;
   const int64_t ntok_max = (a.T + grid - 1) / grid;
   fit(ntok_max);
+  // staged mode with enough tokens per CTA: the tail comes from the counter
+  a.nstat = 0;
+  const int64_t per = a.T / grid;
+  if (a.mode != kModeIdentity && !a.direct && a.queue != nullptr && a.K <= 32 &&
+      per >= kTailMinTokens)
+    a.nstat = (int32_t)(per - (CPT == 1 ? 1 : (per * kTailPct + 99) / 100));
   const size_t smem = smem_bytes(a, ntok_max, bd, CPT);
   err = opt_in_smem(quant_scatter_kernel<GSZ, FMT, CPT>, smem);
   if (err != cudaSuccess) return err;

@@ -827,6 +827,32 @@ def test_dispatch_direct_token_counter(dev, ref, n_live):
     compact_both(dev, ref, x, ids, w, H, K, E, L, 128, 32, "mx", n_live=n_live)
 
 
+@pytest.mark.parametrize("case", ["all_local", "live_count", "remote_tokens"])
+def test_dispatch_staged_tail_from_counter(dev, ref, case):
+    """Rows of two chunks per scatter thread (H = 5248) and 8192 tokens: with
+    at most 4 scatter CTAs per SM on 152 SMs every CTA has at least 13 tokens,
+    so the staged scatter takes its last tokens' worth from the counter that
+    the route plan resets. Cases: every expert local; a device live count
+    that ends inside the counter's range; 128 of 256 experts local with a
+    quarter of the tokens routed only to remote experts (claimed tokens with
+    no kept slot are skipped), compact and masked."""
+    rng = np.random.default_rng(57 + len(case))
+    T, K, E, H = 8192, 8, 256, 5248
+    x = synth.normal_bf16(rng, (T, H), outlier_frac=0.01)
+    ids = synth.uniform_topk(rng, T, E, K)
+    w = synth.softmax_weights(rng, T, K)
+    if case == "all_local":
+        compact_both(dev, ref, x, ids, w, H, K, E, E, 128, 128, "packed")
+    elif case == "live_count":
+        compact_both(dev, ref, x, ids, w, H, K, E, E, 128, 128, "packed", n_live=7900)
+    else:
+        L = 128
+        remote = rng.random(T) < 0.25
+        ids[remote] = L + synth.uniform_topk(rng, int(remote.sum()), E - L, K)
+        compact_both(dev, ref, x, ids, w, H, K, E, L, 128, 128, "packed")
+        masked_both(dev, ref, x, ids, w, H, K, E, L, 384, 128, "u8")
+
+
 @pytest.mark.parametrize("T,L", [(375, 16), (5000, 64), (12500, 64), (25000, 64), (50000, 64)])
 def test_dispatch_route_chain_lengths(dev, ref, T, L):
     rng = np.random.default_rng(T + L)
