@@ -89,15 +89,25 @@ constexpr int kPrefetchAfterWait = 6;
 // tokens per CTA, a CTA's last tokens' worth are not assigned statically but
 // taken from a counter once its static tokens are done, so that CTAs on
 // faster SMs take more of them (per-CTA loop ends on the prefill spread from
-// 83 to 99 us, SM by SM). Wide rows (two chunks per thread) leave
-// ceil(kTailPct% of T / grid) tokens per CTA to the tail, narrow rows one.
-// Dispatch us, tail 0 / 1 / 3 / 8 / 9 / 32 tokens per CTA: T = 8192, H = 7168
-// (17 per CTA) 103.8 / 103.2 / 102.3 / 101.1-101.3 / 100.9 / -; T = 32768
-// (71 per CTA) 391.5 / 389.0 / 383.6 / 381.0 / 380.7 / 373.2; T = 4096
-// (8 per CTA) 57.8 / 58.2 / 62.0; narrow rows, tail 0 / 1 / 3: H = 4096
-// 66.3 / 62.4 / 64.0, H = 5120 64.9 / 64.5 / 65.6, H = 2048 55.6 / 53.8 / 55.7.
+// 83 to 99 us, SM by SM). How many (tail_tokens below) depends on the work
+// per token, f = K * L / E kept slots expected per row: every slot kept
+// (f >= 7.5, wide rows) takes kTailPct% of the CTA's tokens; fewer kept slots
+// take one token per kTailDiv (one fewer below f = 5.5); narrow rows one.
+// Dispatch us, H = 7168, tail tokens per CTA none / 1 / 2 / 4 / 45%:
+//   T = 8192 (17 per CTA): f = 8 105.3 / 103.0 / 102.5 / 102.1 / 101.3;
+//     f = 7 98.3 / 93.1 / 92.8 / 92.5 / 94.3; f = 6 86.9 / 85.3 / 85.2 /
+//     87.2 / 89.6; f = 5 77.7 / 79.3 / 78.5 / 79.6 / 79.0; f = 4 67.8 /
+//     70.2 / 71.6 / 73.2 / 73.6;
+//   T = 16384, f = 4: 128.8 / 126.1 / 125.9 / 126.7 / 131.4;
+//   T = 32768 (71 per CTA): f = 4 247.7 / 243.0 / 240.1 / 239.5 / 249.2;
+//     f = 6 331.2 / 325.5 / 322.0 / 314.8 / 322.1; f = 8 391.5 / 389.0 /
+//     387.1 / 382.4 (5) / 373.2 (32);
+//   T = 4096 (8 per CTA), f = 8: 57.8 / 58.2 / 59.9.
+//   Narrow rows (one chunk per thread), none / 1 / 3: H = 4096 66.3 / 62.4 /
+//   64.0, H = 5120 64.9 / 64.5 / 65.6, H = 2048 55.6 / 53.8 / 55.7.
 constexpr int kTailMinTokens = 12;
 constexpr int kTailPct = 45;
+constexpr int kTailDiv = 17;
 // Direct stores instead of staging when the expected kept slots per token,
 // K * L / E (uniform routing), are at most this many (staged -> direct at
 // T = 8192, H = 7168: f = 1 47.1 -> 43.0 us, f = 3 62.9 -> 61.5, f = 4
@@ -771,8 +781,16 @@ cudaError_t launch_one(const ScatterArgs& a0, int num_sms, bool pdl, cudaStream_
   a.nstat = 0;
   const int64_t per = a.T / grid;
   if (a.mode != kModeIdentity && !a.direct && a.queue != nullptr && a.K <= 32 &&
-      per >= kTailMinTokens)
-    a.nstat = (int32_t)(per - (CPT == 1 ? 1 : (per * kTailPct + 99) / 100));
+      per >= kTailMinTokens) {
+    const int64_t kl2 = 2 * (int64_t)a.K * a.L;  // 2 f E
+    int64_t tail_tokens = 1;
+    if (CPT == 2) {
+      if (kl2 >= 15 * (int64_t)a.E) tail_tokens = (per * kTailPct + 99) / 100;
+      else if (kl2 >= 11 * (int64_t)a.E) tail_tokens = per / kTailDiv > 1 ? per / kTailDiv : 1;
+      else tail_tokens = per / kTailDiv - 1;
+    }
+    if (tail_tokens > 0) a.nstat = (int32_t)(per - tail_tokens);
+  }
   const size_t smem = smem_bytes(a, ntok_max, bd, CPT);
   err = opt_in_smem(quant_scatter_kernel<GSZ, FMT, CPT>, smem);
   if (err != cudaSuccess) return err;

@@ -832,10 +832,11 @@ def test_dispatch_staged_tail_from_counter(dev, ref, case):
     """Rows of two chunks per scatter thread (H = 5248) and 8192 tokens: with
     at most 4 scatter CTAs per SM on 152 SMs every CTA has at least 13 tokens,
     so the staged scatter takes its last tokens' worth from the counter that
-    the route plan resets. Cases: every expert local; a device live count
-    that ends inside the counter's range; 128 of 256 experts local with a
-    quarter of the tokens routed only to remote experts (claimed tokens with
-    no kept slot are skipped), compact and masked."""
+    the route plan resets. Cases: every expert local (the deep tail), compact
+    and masked; a device live count that ends inside the counter's range;
+    192 of 256 experts local (6 kept slots per token expected: a one-token
+    tail) with a quarter of the tokens routed only to remote experts (claimed
+    tokens with no kept slot are skipped), compact and masked."""
     rng = np.random.default_rng(57 + len(case))
     T, K, E, H = 8192, 8, 256, 5248
     x = synth.normal_bf16(rng, (T, H), outlier_frac=0.01)
@@ -843,10 +844,11 @@ def test_dispatch_staged_tail_from_counter(dev, ref, case):
     w = synth.softmax_weights(rng, T, K)
     if case == "all_local":
         compact_both(dev, ref, x, ids, w, H, K, E, E, 128, 128, "packed")
+        masked_both(dev, ref, x, ids, w, H, K, E, E, 384, 128, "packed")
     elif case == "live_count":
         compact_both(dev, ref, x, ids, w, H, K, E, E, 128, 128, "packed", n_live=7900)
     else:
-        L = 128
+        L = 192
         remote = rng.random(T) < 0.25
         ids[remote] = L + synth.uniform_topk(rng, int(remote.sum()), E - L, K)
         compact_both(dev, ref, x, ids, w, H, K, E, L, 128, 128, "packed")
