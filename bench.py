@@ -446,9 +446,9 @@ def run_ours(args, rank, world, local_rank):
     # Every step copies its inputs (x, ids, weights, expert outputs y) from
     # pinned host memory, runs the two calls and reads the combined output
     # back. Two device buffer sets alternate between steps, so step i+1's
-    # host->device copies (the bulk of the time: ~210 GB/s is this link's
-    # ceiling) overlap step i's compute and its device->host read; y is copied
-    # in two halves on two streams.
+    # host->device copies (the bulk of the time, at the host link's rate,
+    # measured on its own below as h2d_link_gbs) overlap step i's compute and
+    # its device->host read; y is copied in two halves on two streams.
     x_p, ids_p, w_p = x_h.pin_memory(), ids_h.pin_memory(), w_h.pin_memory()
     y_p = y.cpu().pin_memory()
     out_p = [torch.empty((T, H), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
@@ -497,6 +497,14 @@ def run_ours(args, rank, world, local_rank):
     for i in range(2):
         e2e_step(i)
     torch.cuda.synchronize()
+    # the host link on its own: the pinned expert outputs (the bulk of each
+    # step's host->device bytes) copied to the device on one stream
+    lk0, lk1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    lk0.record(main)
+    sets[0]["y"].copy_(y_p, non_blocking=True)
+    lk1.record(main)
+    torch.cuda.synchronize()
+    link_gbs = y_p.numel() * 2 / (lk0.elapsed_time(lk1) * 1e-3) / 1e9
     e2e_steps = max(4, min(K_steps, 10))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(main)
@@ -573,7 +581,9 @@ def run_ours(args, rank, world, local_rank):
                 "api": "moe_dispatch_compact + moe_combine (C ABI), pinned host buffers; two "
                        "device buffer sets alternate so one step's host->device copies overlap "
                        "the previous step's compute and device->host read",
-                "h2d_link_gbs_note": "pinned host->device copies on this box peak near 210 GB/s"},
+                "h2d_link_gbs": link_gbs,
+                "h2d_link_note": "one pinned host->device copy of the expert outputs alone on this "
+                                 "box; the step's host->device bytes / this rate bound the e2e step"},
         "gpu_launches": 3 * K_steps,
         "clocks": clk,
         "rows": rows,

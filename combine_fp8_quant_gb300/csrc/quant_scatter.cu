@@ -83,8 +83,10 @@ static_assert(kCpt1MaxH <= 16384, "one chunk per thread covers at most 1024 x 16
 // while the CTA builds the layout instead of delaying the wait (staged path;
 // measured against 2 tokens before the wait: dispatch 105.1-105.8 -> 104.0-104.4 us,
 // step 266.9-267.7 -> 265.6-266.1 us; 2 / 4 / 8 / 10 / 14 after the wait:
-// 104.7 / 104.6 / 105.1 / 104.8 / 108.1 us).
-constexpr int kPrefetchAfterWait = 6;
+// 104.7 / 104.6 / 105.1 / 104.8 / 108.1 us). With the counter tail, 3 / 6 / 9 /
+// 12: prefill 103.5-104.2 / 100.6-101.3 / 99.9-100.7 / 100.6; the other
+// shape-sweep shapes 0.4-1.7 us faster with 9 than with 6, 12 within 0.4 of 9.
+constexpr int kPrefetchAfterWait = 9;
 // Staged mode, tail from the token counter: with at least kTailMinTokens
 // tokens per CTA, a CTA's last tokens' worth are not assigned statically but
 // taken from a counter once its static tokens are done, so that CTAs on
