@@ -827,7 +827,7 @@ def test_dispatch_direct_token_counter(dev, ref, n_live):
     compact_both(dev, ref, x, ids, w, H, K, E, L, 128, 32, "mx", n_live=n_live)
 
 
-@pytest.mark.parametrize("case", ["all_local", "live_count", "remote_tokens"])
+@pytest.mark.parametrize("case", ["all_local", "live_count", "remote_tokens", "overflow", "top6"])
 def test_dispatch_staged_tail_from_counter(dev, ref, case):
     """Rows of two chunks per scatter thread (H = 5248) and 8192 tokens: with
     at most 4 scatter CTAs per SM on 152 SMs every CTA has at least 13 tokens,
@@ -836,7 +836,10 @@ def test_dispatch_staged_tail_from_counter(dev, ref, case):
     and masked; a device live count that ends inside the counter's range;
     192 of 256 experts local (6 kept slots per token expected: a one-token
     tail) with a quarter of the tokens routed only to remote experts (claimed
-    tokens with no kept slot are skipped), compact and masked."""
+    tokens with no kept slot are skipped), compact and masked; a masked
+    capacity below the busiest experts' counts (rows past it dropped, the
+    overflow flag set) with the deep tail; top-6 of 160 local experts (the
+    count-scaled tail)."""
     rng = np.random.default_rng(57 + len(case))
     T, K, E, H = 8192, 8, 256, 5248
     x = synth.normal_bf16(rng, (T, H), outlier_frac=0.01)
@@ -847,6 +850,13 @@ def test_dispatch_staged_tail_from_counter(dev, ref, case):
         masked_both(dev, ref, x, ids, w, H, K, E, E, 384, 128, "packed")
     elif case == "live_count":
         compact_both(dev, ref, x, ids, w, H, K, E, E, 128, 128, "packed", n_live=7900)
+    elif case == "overflow":
+        masked_both(dev, ref, x, ids, w, H, K, E, E, 256, 128, "packed")
+    elif case == "top6":
+        K6, E6 = 6, 160
+        ids6 = synth.uniform_topk(rng, T, E6, K6)
+        w6 = synth.softmax_weights(rng, T, K6)
+        compact_both(dev, ref, x, ids6, w6, H, K6, E6, E6, 128, 128, "packed")
     else:
         L = 192
         remote = rng.random(T) < 0.25
