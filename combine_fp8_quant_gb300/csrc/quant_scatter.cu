@@ -70,7 +70,10 @@ namespace {
 // tokens quantised before the wait on the route plan; the launch lowers both
 // when shared memory is short (large H with a large chunk table). Measured on
 // the prefill workload: 4 buffers / 2 early tokens 102.7-103.0 us, 3 / 2
-// 105.6, 5 / 2 106.7 (5 buffers drop to 3 CTAs per SM), 6 / 4 104.2.
+// 105.6, 5 / 2 106.7 (5 buffers drop to 3 CTAs per SM), 6 / 4 104.2; with the
+// post-wait prefetch 4 / 2 105.1-105.6, 4 / 1, 4 / 3 and 5 / 2 within 0.4 us,
+// 3 / 2 109.6-110.3; with the counter tail 4 / 1 102.4-102.6 against
+// 100.8-101.1.
 constexpr int kStages = 4;
 constexpr int kPre = 2;
 // Rows up to this width take one 16-element chunk per thread (twice the
@@ -567,7 +570,7 @@ __global__ void __launch_bounds__(1024, 1) quant_scatter_kernel(ScatterArgs p) {
     nlist = 0;  // nothing left for the staged loop below
   }
 
-  // ---- token loop ---------------------------------------------------------
+  // ---- token loop (dispatch modes; the identity mode returned above) --------
   // The quantised row is staged in shared memory (p.stages rotating buffers)
   // and thread 0 writes it to every destination row with bulk copies, so the
   // payload stores leave the SM as a few large TMA transfers. One barrier per
@@ -641,7 +644,8 @@ __global__ void __launch_bounds__(1024, 1) quant_scatter_kernel(ScatterArgs p) {
   }
 
   // ---- tail: tokens [nstat * grid, n_live) from the counter the route plan
-  // reset, each taken exactly once. Warp 0 claims the next token with a kept
+  // reset, each taken exactly once (which CTA takes a token changes no
+  // output: its rows follow from the layout alone). Warp 0 claims the next token with a kept
   // slot and resolves its rows (rewriting its src2dst entries) into the other
   // of two ring entries while the current token is quantised; the staging
   // ring and its barrier continue from the static loop. Claiming only one
