@@ -748,6 +748,67 @@ def test_graph_capture_replay_new_routing(dev, ref):
     assert int(st.item()) == 0
 
 
+def test_graph_capture_replay_with_counter_tail(dev, ref):
+    """The dispatch captured once at a size where the staged scatter takes
+    its last tokens from the counter (8192 tokens, H = 5248, every expert
+    local), then replayed on new routing: the route plan inside the graph
+    resets the counter on every replay, and every output buffer (padding rows
+    pre-filled with sentinels) matches the oracle."""
+    T, H, K, E, L, b, g = 8192, 5248, 8, 256, 256, 128, 128
+    G = H // g
+    bound = ref.compact_bound(T * K, L, b)
+    sent = {"xq": np.full((bound, H), 0xEE, np.uint8)}
+    sent["sc"], ld = ref.scale_buffer("packed", bound, G, fill=0xA5)
+    sent["mi"] = np.full(bound, -7, np.int32)
+    sent["s2d"] = np.full((T, K), -9, np.int32)
+    for k in ("counts", "starts", "psum"):
+        sent[k] = np.full(L, -5, np.int32)
+    sent["total"] = np.full(1, -3, np.int32)
+    sent["rw"] = np.full(bound, np.nan, np.float32)
+    d = {k: to_dev(v.copy()) for k, v in sent.items()}
+    rng = np.random.default_rng(71)
+    x = bf16_dev(synth.normal_bf16(rng, (T, H)))
+    ids = to_dev(synth.uniform_topk(rng, T, E, K))
+    w = to_dev(synth.softmax_weights(rng, T, K))
+    ws = dev.Workspace(T, K, L, DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+
+    def call():
+        assert dev.moe_dispatch_compact(x, H, T, None, H, ids, w, K, E, L, b, g, "packed", d["xq"],
+                                        d["sc"], ld, d["mi"], bound, d["s2d"], d["counts"],
+                                        d["starts"], d["psum"], d["total"], d["rw"], ws.buf,
+                                        ws.nbytes, st) == dev.MOE_OK
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        call()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call()
+    for seed in (1, 2):
+        rn = np.random.default_rng(71 + seed)
+        xh = synth.normal_bf16(rn, (T, H))
+        idh = synth.uniform_topk(rn, T, E, K)
+        wh = synth.softmax_weights(rn, T, K)
+        x.copy_(bf16_dev(xh))
+        ids.copy_(to_dev(idh))
+        w.copy_(to_dev(wh))
+        for k, v in sent.items():
+            d[k].copy_(to_dev(v))
+        graph.replay()
+        torch.cuda.synchronize()
+        r = {k: v.copy() for k, v in sent.items()}
+        st_ref = ref.dispatch_compact(xh, T, T, H, idh, wh, K, L, b, g, "packed", r["xq"], r["sc"],
+                                      ld, r["mi"], bound, r["s2d"], r["counts"], r["starts"],
+                                      r["psum"], r["total"], r["rw"])
+        assert st_ref == 0
+        for k, v in r.items():
+            assert_same(f"replay {seed}: {k}", to_host(d[k], v), v)
+    assert int(st.item()) == 0
+
+
 def test_graph_capture_scatter_above_48k_shared_memory(dev, ref):
     """Capture of a two-launch dispatch whose scatter CTA needs more than the
     default 48 KiB of shared memory (1024 experts, 15 chunks: a 60 KiB chunk
