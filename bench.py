@@ -635,11 +635,42 @@ def load_traffic(which):
     return None
 
 
-def time_call(fn, flush, reps=40):
+class NvtxRange:
+    """An NVTX range around a timed row, so that a profiler capture can select
+    one row's launches (ncu --nvtx --nvtx-include "<name>/"); a no-op where
+    NVTX is unavailable."""
+
+    def __init__(self, name):
+        self.name, self.pushed = name, False
+
+    def __enter__(self):
+        if self.name:
+            try:
+                import torch
+                torch.cuda.nvtx.range_push(self.name)
+                self.pushed = True
+            except Exception:
+                self.pushed = False
+        return self
+
+    def __exit__(self, *exc):
+        if self.pushed:
+            import torch
+            torch.cuda.nvtx.range_pop()
+        return False
+
+
+def time_call(fn, flush, reps=40, name=None):
     """Device time of one call in us, L2 flushed before each: the mean of
     `reps` CUDA-event intervals with the top and bottom 10% dropped. Events on
     this GPU tick in steps of about 2 us, so a median would snap to a tick;
-    the trimmed mean averages over the quantisation."""
+    the trimmed mean averages over the quantisation. `name` labels the calls
+    with an NVTX range."""
+    with NvtxRange(name):
+        return _time_call(fn, flush, reps)
+
+
+def _time_call(fn, flush, reps):
     import torch
     for _ in range(3):
         fn()
@@ -725,10 +756,10 @@ def other_rows(mp, dev, flush):
     nb_from = nb_repack + R * 4                           # + m_indices over the expanded rows
     nb_to = nb_repack + L * 4                             # + masked_m
     nb_comb = kept * H * 2 + T * K * 8 + T * H * 2
-    res["decode_masked_dispatch"] = entry(time_call(dec, flush), nb_disp)
-    res["decode_slab_to_expand"] = entry(time_call(from_slab, flush), nb_from)
-    res["decode_expand_to_slab"] = entry(time_call(to_slab, flush), nb_to)
-    res["decode_combine_from_slab"] = entry(time_call(decomb, flush), nb_comb)
+    res["decode_masked_dispatch"] = entry(time_call(dec, flush, name="decode_masked_dispatch"), nb_disp)
+    res["decode_slab_to_expand"] = entry(time_call(from_slab, flush, name="decode_slab_to_expand"), nb_from)
+    res["decode_expand_to_slab"] = entry(time_call(to_slab, flush, name="decode_expand_to_slab"), nb_to)
+    res["decode_combine_from_slab"] = entry(time_call(decomb, flush, name="decode_combine_from_slab"), nb_comb)
     # the whole decode chain, captured once, as one graph replay
     dec(), from_slab(), to_slab(), decomb()
     torch.cuda.synchronize()
@@ -738,7 +769,7 @@ def other_rows(mp, dev, flush):
         from_slab()
         to_slab()
         decomb()
-    res["decode_chain_graph"] = entry(time_call(gchain.replay, flush),
+    res["decode_chain_graph"] = entry(time_call(gchain.replay, flush, name="decode_chain_graph"),
                                       nb_disp + nb_from + nb_to + nb_comb)
     res["decode_chain_graph"]["launches"] = 4
     res["decode_chain_graph"]["expanded_rows"] = R
@@ -755,7 +786,7 @@ def other_rows(mp, dev, flush):
     def mx():
         assert mp.moe_quant_group(xb, cm["H"], cm["T_cap"], nl, cm["H"], 32, "u8", xqm, scm,
                                   cm["H"] // 32, st) == 0
-    us = time_call(mx, flush)
+    us = time_call(mx, flush, name="mxfp8_live_quant")
     res["mxfp8_live_quant"] = entry(us, cm["n_live"] * cm["H"] * 3 + cm["n_live"] * 224)
     res["mxfp8_live_quant"]["capacity_rows"] = cm["T_cap"]
     # the same quantiser on a full prefill batch (8192 rows, group 128, packed)
@@ -766,7 +797,7 @@ def other_rows(mp, dev, flush):
 
     def qf():
         assert mp.moe_quant_group(xf, Hq, Tq, None, Hq, 128, "packed", xqf, scf, ldf, st) == 0
-    res["quant_group_prefill"] = entry(time_call(qf, flush), Tq * Hq * 3 + Tq * (Hq // 128))
+    res["quant_group_prefill"] = entry(time_call(qf, flush, name="quant_group_prefill"), Tq * Hq * 3 + Tq * (Hq // 128))
     res["quant_group_prefill"]["rows"] = Tq
     del xf, xqf, scf
 
@@ -785,7 +816,7 @@ def other_rows(mp, dev, flush):
 
         def rq():
             assert mp.fp8_requant_per_tensor(q, H, s, T, H, qo, S) == 0
-        res["requant_per_tensor" + tag] = entry(time_call(rq, flush), 2 * T * H + T * 4 + 4)
+        res["requant_per_tensor" + tag] = entry(time_call(rq, flush, name="requant_per_tensor" + tag), 2 * T * H + T * 4 + 4)
         res["requant_per_tensor" + tag]["rows"] = T
 
         counts = synth.repack_counts(np.random.default_rng(17 + rep), cr["L"], cr["blocks"] * rep,
@@ -815,8 +846,8 @@ def other_rows(mp, dev, flush):
             assert mp.moe_expand_from_slab(slab, 1, H, ssc, ld_ss, psum, cr["L"], 128, capr,
                                            "packed", 128, None, back, R, esc, ld_es, mi, st) == 0
         nb = 2 * real * (H + ((G + 3) // 4) * 4) + cr["L"] * 8
-        res["expand_to_slab" + tag] = entry(time_call(to_slab, flush), nb)
-        res["slab_to_expand" + tag] = entry(time_call(from_slab, flush), nb + R * 4)
+        res["expand_to_slab" + tag] = entry(time_call(to_slab, flush, name="expand_to_slab" + tag), nb)
+        res["slab_to_expand" + tag] = entry(time_call(from_slab, flush, name="slab_to_expand" + tag), nb + R * 4)
         res["expand_to_slab" + tag]["real_rows"] = real
         del q, qo, slab, back
     torch.cuda.synchronize()
@@ -978,6 +1009,19 @@ def only_dispatch(args):
     print(json.dumps({"only_dispatch": True, "T": T, "calls": args.warmup + args.steps}), flush=True)
 
 
+def only_rows(args):
+    """The other hot-path rows alone (no prefill step, e2e or CPU baseline),
+    each labelled with an NVTX range; for profiler captures of their kernels."""
+    import torch
+    import combine_fp8_quant_gb300 as mp
+    from combine_fp8_quant_gb300 import build as cuda_build
+    cuda_build.build()
+    mp.load()
+    dev = torch.device("cuda:0")
+    rows = other_rows(mp, dev, L2Flush(dev))
+    print(json.dumps({"only_rows": True, "rows": rows}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -990,6 +1034,9 @@ def main():
     ap.add_argument("--only-dispatch", action="store_true",
                     help="run W + K prefill dispatch calls and nothing else; for profiler "
                          "captures of the dispatch kernels")
+    ap.add_argument("--only-rows", action="store_true",
+                    help="time the other hot-path rows only, each in an NVTX range named after its "
+                         "row; for profiler captures of their kernels")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override T of the prefill workload (profiling smaller cases)")
     ap.add_argument("--layout-sweep", action="store_true",
@@ -999,6 +1046,9 @@ def main():
     args = ap.parse_args()
     if args.only_dispatch:
         only_dispatch(args)
+        return
+    if args.only_rows:
+        only_rows(args)
         return
     if args.layout_sweep:
         layout_sweep(args)
