@@ -950,11 +950,13 @@ def test_dispatch_long_route_chain(dev, ref):
     masked_both(dev, ref, x, ids, w, H, K, L, L, 256, 128, "packed")
 
 
-@pytest.mark.parametrize("T,K", [(9, 2), (1100, 2), (1100, 4)])  # one launch; two launches,
-def test_dispatch_max_hidden(dev, ref, T, K):                       # direct (K*L/E = 2) or staged (4)
+# one launch; two launches: direct (K*L/E = 2), staged (4), staged with the counter tail (8)
+@pytest.mark.parametrize("T,K", [(9, 2), (1100, 2), (1100, 4), (2000, 8)])
+def test_dispatch_max_hidden(dev, ref, T, K):
     """H = 32768: the two-launch scatter covers the row with 1024 threads x 2
     chunks of 16 in one pass (staged: four 32 KiB staging buffers); the
-    one-launch path loops four passes."""
+    one-launch path loops four passes. With 2000 tokens and every slot kept, a
+    CTA per SM has 13 tokens and takes the last ones from the counter."""
     rng = np.random.default_rng(21 + K)
     L, H = 8, 32768
     x = synth.normal_bf16(rng, (T, H), outlier_frac=0.01)
