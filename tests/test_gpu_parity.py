@@ -888,7 +888,8 @@ def test_dispatch_direct_token_counter(dev, ref, n_live):
     compact_both(dev, ref, x, ids, w, H, K, E, L, 128, 32, "mx", n_live=n_live)
 
 
-@pytest.mark.parametrize("case", ["all_local", "live_count", "remote_tokens", "overflow", "top6"])
+@pytest.mark.parametrize("case", ["all_local", "live_count", "remote_tokens", "overflow", "top6",
+                                  "narrow_masked"])
 def test_dispatch_staged_tail_from_counter(dev, ref, case):
     """Rows of two chunks per scatter thread (H = 5248) and 8192 tokens: with
     at most 4 scatter CTAs per SM on 152 SMs every CTA has at least 13 tokens,
@@ -900,7 +901,9 @@ def test_dispatch_staged_tail_from_counter(dev, ref, case):
     tokens with no kept slot are skipped), compact and masked; a masked
     capacity below the busiest experts' counts (rows past it dropped, the
     overflow flag set) with the deep tail; top-6 of 160 local experts (the
-    count-scaled tail)."""
+    count-scaled tail); and rows of one chunk per thread (H = 2048, 16384
+    tokens, top-6 of 64: the one-token tail), masked, with a device live
+    count."""
     rng = np.random.default_rng(57 + len(case))
     T, K, E, H = 8192, 8, 256, 5248
     x = synth.normal_bf16(rng, (T, H), outlier_frac=0.01)
@@ -913,6 +916,12 @@ def test_dispatch_staged_tail_from_counter(dev, ref, case):
         compact_both(dev, ref, x, ids, w, H, K, E, E, 128, 128, "packed", n_live=7900)
     elif case == "overflow":
         masked_both(dev, ref, x, ids, w, H, K, E, E, 256, 128, "packed")
+    elif case == "narrow_masked":
+        Tn, Hn, Kn, En = 16384, 2048, 6, 64
+        xn = synth.normal_bf16(rng, (Tn, Hn))
+        idn = synth.uniform_topk(rng, Tn, En, Kn)
+        wn = synth.softmax_weights(rng, Tn, Kn)
+        masked_both(dev, ref, xn, idn, wn, Hn, Kn, En, En, 2048, 128, "packed", n_live=16000)
     elif case == "top6":
         K6, E6 = 6, 160
         ids6 = synth.uniform_topk(rng, T, E6, K6)
