@@ -184,6 +184,9 @@ size_t moe_workspace_bytes(int32_t T, int32_t K, int32_t L);
  * the layout + quantise + scatter + m_indices launch. The second is started
  * early with programmatic dependent launch: its CTAs quantise their first
  * tokens while the route plan runs and wait for its results on the device.
+ * With enough tokens per CTA its last tokens are handed out through a counter
+ * in the workspace (reset by the route plan), so that which CTA handles a
+ * token varies between calls; no output depends on it.
  */
 moe_status_t moe_dispatch_compact(
     const void* x, int64_t ldx, int32_t T, const int32_t* d_num_tokens, int32_t H,
