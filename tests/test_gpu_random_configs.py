@@ -125,3 +125,36 @@ def test_random_wide_configs(dev, ref, seed):
     cap = max(1, top if rng.random() < 0.7 else top // 2)
     if L * cap * H <= 200_000_000:
         masked_both(dev, ref, x, ids, w, H, K, E, L, cap, g, fmt)
+
+
+def draw_tail(rng):
+    """Sizes where the staged scatter takes its last tokens from the counter:
+    7300-12000 tokens of rows wider than 5120 elements (two chunks per thread:
+    at most 4 CTAs per SM on 152 SMs, so at least 12 tokens per CTA), top-6..8
+    with at least 5.5 kept slots expected per token (K*L/E), where even 12
+    tokens per CTA take a tail."""
+    H = 128 * int(rng.integers(41, 61))                  # 5248 .. 7680
+    T = int(rng.integers(7300, 12001))
+    K = int(rng.integers(6, 9))
+    E = int(rng.choice([64, 128, 256]))
+    L = int(rng.integers(-(-11 * E // (2 * K)), E + 1))  # K*L/E >= 5.5
+    return H, T, K, L, E
+
+
+# Seeded draws in the counter tail's range, every slot kept or not, compact
+# and masked, with device live counts on half of them.
+@pytest.mark.parametrize("seed", range(4))
+def test_random_tail_configs(dev, ref, seed):
+    rng = np.random.default_rng(72000 + seed)
+    H, T, K, L, E = draw_tail(rng)
+    fmt = str(rng.choice(["packed", "u8"]))
+    n_live = None if seed % 2 == 0 else int(rng.integers(T // 2, T + 1))
+    ids = random_routing(rng, T, E, K)
+    w = synth.softmax_weights(rng, T, K)
+    x = synth.normal_bf16(rng, (T, H), outlier_frac=0.01)
+    compact_both(dev, ref, x, ids, w, H, K, E, L, 128, 128, fmt, n_live=n_live)
+    kept = ids[(ids >= 0) & (ids < L)]
+    top = int(np.bincount(kept, minlength=L).max()) if kept.size else 0
+    cap = max(1, top if seed < 2 else (3 * top) // 4)
+    if L * cap * H <= 600_000_000:
+        masked_both(dev, ref, x, ids, w, H, K, E, L, cap, 128, fmt, n_live=n_live)
