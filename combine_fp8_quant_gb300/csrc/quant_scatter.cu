@@ -107,10 +107,12 @@ constexpr int kPrefetchAfterWait = 9;
 //   T = 32768 (71 per CTA): f = 4 247.7 / 243.0 / 240.1 / 239.5 / 249.2;
 //     f = 6 331.2 / 325.5 / 322.0 / 314.8 / 322.1; f = 8 391.5 / 389.0 /
 //     387.1 / 382.4 (5) / 373.2 (32);
-//   T = 4096 (8 per CTA), f = 8: 57.8 / 58.2 / 59.9.
+//   T = 4096 (8 per CTA), f = 8: 57.8 / 58.2 / 59.9. Tokens per CTA 12 / 13 /
+//   16, f = 8, no tail against the 45% tail: 72.3-72.6 / 80.9-81.0 / 94.3-94.6
+//   against 73.2-73.6 / 78.7-79.4 / 90.0-90.1.
 //   Narrow rows (one chunk per thread), none / 1 / 3: H = 4096 66.3 / 62.4 /
 //   64.0, H = 5120 64.9 / 64.5 / 65.6, H = 2048 55.6 / 53.8 / 55.7.
-constexpr int kTailMinTokens = 12;
+constexpr int kTailMinTokens = 13;
 constexpr int kTailPct = 45;
 constexpr int kTailDiv = 17;
 // Direct stores instead of staging when the expected kept slots per token,

@@ -129,12 +129,12 @@ def test_random_wide_configs(dev, ref, seed):
 
 def draw_tail(rng):
     """Sizes where the staged scatter takes its last tokens from the counter:
-    7300-12000 tokens of rows wider than 5120 elements (two chunks per thread:
-    at most 4 CTAs per SM on 152 SMs, so at least 12 tokens per CTA), top-6..8
-    with at least 5.5 kept slots expected per token (K*L/E), where even 12
+    7904-12000 tokens of rows wider than 5120 elements (two chunks per thread:
+    at most 4 CTAs per SM on 152 SMs, so at least 13 tokens per CTA), top-6..8
+    with at least 5.5 kept slots expected per token (K*L/E), where even 13
     tokens per CTA take a tail."""
     H = 128 * int(rng.integers(41, 61))                  # 5248 .. 7680
-    T = int(rng.integers(7300, 12001))
+    T = int(rng.integers(7904, 12001))
     K = int(rng.integers(6, 9))
     E = int(rng.choice([64, 128, 256]))
     L = int(rng.integers(-(-11 * E // (2 * K)), E + 1))  # K*L/E >= 5.5
